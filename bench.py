@@ -1,0 +1,392 @@
+#!/usr/bin/env python
+"""Benchmark of the Periodic Row-wise Muon optimizer step on one GB300 (or N replicas).
+
+One bench step = one period of the K = 3 schedule over the whole parameter set:
+an NS5 refresh step followed by two RowNorm steps (every row of the hot path:
+schedule, momentum, Newton-Schulz, RowNorm, scale, apply).  The reported value is
+the mean optimizer-step time (period / 3).  Inputs (W, G, M) are synthetic, on the
+device before the timed region, and larger than L2.  Newton-Schulz GEMM time and
+RowNorm time come from CUDA events that the library records on its stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Muon optimizer step ms; NS5 TFLOP/s and RowNorm GB/s vs GB300 roofline"
+DEFAULT_WORKLOAD = "mmdit-1.3b"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129e6
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# analytic work
+# ---------------------------------------------------------------------------
+def ns5_flops(shapes):
+    """Dense count 5*(4 n^2 m + 2 n^3) per matrix, n = min(A, B), m = max(A, B)."""
+    return sum(5 * (4 * min(a, b) ** 2 * max(a, b) + 2 * min(a, b) ** 3) for a, b in shapes)
+
+
+def ns5_flops_executed(shapes):
+    """FLOPs the tensor-core kernels issue: 128x256 output tiles with K padded to 64;
+    for the two symmetric products only the tiles that touch the upper triangle
+    (row blocks up to 2*tn+1 of each 256-column block)."""
+    tot = 0
+    for a, b in shapes:
+        n, m = min(a, b), max(a, b)
+        mt = -(-n // 128)
+        sym = sum(min(2 * t + 2, mt) for t in range(-(-n // 256)))
+        kn, km = 64 * -(-n // 64), 64 * -(-m // 64)
+        tile = 2 * 128 * 256
+        tot += 5 * tile * (sym * km + sym * kn + mt * -(-m // 256) * kn)
+    return tot
+
+
+def rownorm_bytes(shapes, wb, gb):
+    """Algorithmic bytes of a RowNorm step: read G, read+write M (fp32), read+write W."""
+    return sum(a * b * (gb + 8 + 2 * wb) for a, b in shapes)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas: no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_init(torch):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, None
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend)
+    return dist.get_rank(), dist.get_world_size(), dist
+
+
+def max_over_ranks(torch, dist, x: float, device) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# oracle (CPU) timing on a bounded sample
+# ---------------------------------------------------------------------------
+def oracle_sample(wl, seed=0):
+    """One matrix per shape group through one K=3 period with the fp64 oracle.
+    Returns the extrapolated ms per optimizer step for the whole set, and details."""
+    import numpy as np
+    from oracle import muon_ref
+    from synth import gradient_np, quantize_np, weight_init_np
+    groups = wl.shape_groups()
+    total = 0.0
+    detail = []
+    for gi, ((a, b), cnt) in enumerate(groups):
+        W = quantize_np(weight_init_np(a, b, seed, gi), wl.w_dtype).astype(np.float64)
+        M = np.zeros((a, b))
+        ts = []
+        for step in range(wl.K):
+            G = quantize_np(gradient_np(a, b, wl.spike_scales, seed, gi, step), wl.g_dtype)
+            t0 = time.perf_counter()
+            W, M, _ = muon_ref.periodic_step(W, M, G, step, wl.K, wl.gamma, wl.mu, wl.eta, wl.lam,
+                                             w_dtype=wl.w_dtype)
+            ts.append(time.perf_counter() - t0)
+        total += cnt * sum(ts) / wl.K
+        detail.append({"shape": [a, b], "count": cnt, "refresh_s": round(ts[0], 4),
+                       "rownorm_s": round(sum(ts[1:]) / max(len(ts) - 1, 1), 4)})
+    return total * 1e3, detail
+
+
+def run_reference(args, torch):
+    rank, world, dist = dist_init(torch)
+    if rank != 0:
+        return
+    from synth import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    for _ in range(min(args.warmup, 1)):   # the oracle needs no more warm-up than one pass
+        oracle_sample(wl)
+    vals = []
+    for _ in range(args.steps):
+        v, detail = oracle_sample(wl)
+        vals.append(v)
+    value = statistics.mean(vals)
+    sample = (f"one matrix per shape group ({len(wl.shape_groups())} groups) through one K={wl.K} period, "
+              f"extrapolated by group counts to {len(wl.matrices)} matrices")
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "ms", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value * wl.K, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.key, "matrices": len(wl.matrices), "params": wl.n_params, "K": wl.K,
+                       "gamma": wl.gamma, "parallelism": "replicas"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "ms", "cores": cores, "kind": "oracle",
+                             "sample": sample, "detail": detail},
+            "e2e": {"value": round(value, 3), "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+def run_ours(args, torch):
+    import matrix_aware_optimizer_muon_gb300 as mm
+    from synth import WORKLOADS, gradient_torch, weight_init_torch
+
+    rank, world, dist = dist_init(torch)
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    mm.load_library()
+    wl = WORKLOADS[args.workload]
+    shapes = [(m.rows, m.cols) for m in wl.matrices]
+    wdt = torch.bfloat16 if wl.w_dtype == "bf16" else torch.float32
+    gdt = torch.bfloat16 if wl.g_dtype == "bf16" else torch.float32
+    wb, gb = (2 if wl.w_dtype == "bf16" else 4), (2 if wl.g_dtype == "bf16" else 4)
+
+    # flat device buffers (one H2D / D2H copy each for the end-to-end run)
+    offs, tot = [], 0
+    for a, b in shapes:
+        offs.append(tot)
+        tot += -(-(a * b) // 128) * 128
+    W_flat = torch.empty(tot, dtype=wdt, device=device)
+    G_flat = torch.empty(tot, dtype=gdt, device=device)
+    M_flat = torch.zeros(tot, dtype=torch.float32, device=device)
+    W = [W_flat[o:o + a * b].view(a, b) for o, (a, b) in zip(offs, shapes)]
+    G = [G_flat[o:o + a * b].view(a, b) for o, (a, b) in zip(offs, shapes)]
+    M = [M_flat[o:o + a * b].view(a, b) for o, (a, b) in zip(offs, shapes)]
+    seed = 1234 + rank
+    for i, (a, b) in enumerate(shapes):
+        W[i].copy_(weight_init_torch(torch, device, a, b, seed, i, wdt))
+        gradient_torch(torch, device, a, b, wl.spike_scales, seed, i, 0, gdt, out=G[i])
+    ws = mm.alloc_workspace(shapes, "bf16" if wl.w_dtype == "bf16" else "f32", device=device)
+    mode = "bf16" if wl.w_dtype == "bf16" else "f32"
+    stream = torch.cuda.current_stream()
+
+    launches = [0]
+
+    def opt_step(step):
+        mm.muon_periodic_step(W, G, M, step, ws, K=wl.K, gamma=wl.gamma, mu=wl.mu, eta=wl.eta, lam=wl.lam,
+                              ns5_mode=mode)
+        launches[0] += mm.muon_launch_count()
+
+    step_counter = [0]
+
+    def period(evsets=None):
+        for _ in range(wl.K):
+            if evsets is not None:
+                mm.muon_profile_events(evsets)
+            opt_step(step_counter[0])
+            step_counter[0] += 1
+
+    # warm-up (also the first call configures the kernels)
+    for _ in range(args.warmup):
+        period()
+    torch.cuda.synchronize()
+    if mm.muon_check_status(ws) != mm.MUON_OK:
+        raise RuntimeError("device status error during warm-up")
+
+    # timed region: per-period event sets record the phase boundaries
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for s in evs:
+        for e in s:
+            e.record()
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist)
+    torch.cuda.synchronize()
+    launches[0] = 0
+    wall0 = time.perf_counter()
+    t0e.record()
+    for i in range(args.steps):
+        period(evs[i])
+    t1e.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(dist)
+    clk = clocks.stop()
+    mm.muon_profile_events([])
+    if mm.muon_check_status(ws) != mm.MUON_OK:
+        raise RuntimeError("device status error in the timed region")
+    period_ms = t0e.elapsed_time(t1e) / args.steps
+    period_ms = max_over_ranks(torch, dist, period_ms, device)
+    refresh_ms = statistics.mean(s[0].elapsed_time(s[2]) for s in evs)
+    ns5_ms = statistics.mean(s[1].elapsed_time(s[2]) for s in evs)
+    rownorm_ms = statistics.mean(s[3].elapsed_time(s[4]) for s in evs)   # the last RowNorm step of each period
+    gpu_launches = launches[0] // args.steps
+
+    flops = ns5_flops(shapes)
+    flops_exec = ns5_flops_executed(shapes)
+    rn_bytes = rownorm_bytes(shapes, wb, gb)
+    pk, pk_src = peaks()
+    ns5_tflops = flops / (ns5_ms * 1e-3) / 1e12
+    ns5_exec_tflops = flops_exec / (ns5_ms * 1e-3) / 1e12
+    rn_gbs = rn_bytes / (rownorm_ms * 1e-3) / 1e9
+    peak_tc = pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+    peak_hbm = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    n_ns5_launches = 15 * max(1, math.ceil(len(wl.shape_groups()) / 8))
+
+    line = {
+        "metric": METRIC, "value": round(period_ms / wl.K, 4), "unit": "ms", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(period_ms, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if mode == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.key, "matrices": len(shapes), "params": wl.n_params,
+                   "K": wl.K, "gamma": wl.gamma, "mu": wl.mu, "eta": wl.eta, "lambda": wl.lam,
+                   "step": f"one K={wl.K} period: 1 NS5 refresh + {wl.K - 1} RowNorm optimizer steps; value = period/{wl.K}",
+                   "l2": f"inputs larger than L2 (W+G+M {tot * (wb + gb + 4) / 1e9:.1f} GB vs 129 MB L2), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "refresh_ms": round(refresh_ms, 4), "ns5_ms": round(ns5_ms, 4), "rownorm_ms": round(rownorm_ms, 4),
+        "ns5_tflops": round(ns5_tflops, 1), "ns5_tflops_executed": round(ns5_exec_tflops, 1),
+        "rownorm_gbs": round(rn_gbs, 1),
+        "roofline": {"kernel": "ns_tc_kernel (Newton-Schulz GEMMs)", "bound": "tensor",
+                     "achieved": round(ns5_tflops, 1), "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": round(ns5_tflops / peak_tc, 4), "traffic": None,
+                     "peak_source": f"{pk_src} bf16_tflops_sustained",
+                     "frac_of_nominal_2250": round(ns5_tflops / 2250.0, 4),
+                     "flops_per_refresh": flops, "launches_per_refresh": n_ns5_launches},
+        "rownorm_roofline": {"bound": "hbm", "achieved": round(rn_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                             "frac": round(rn_gbs / peak_hbm, 4), "bytes_per_step": rn_bytes,
+                             "peak_source": f"{pk_src} hbm_gbs", "frac_of_nominal_8000": round(rn_gbs / 8000.0, 4)},
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+        "wall_s": round(wall, 3),
+    }
+
+    # end-to-end through the public API with host buffers (pinned), copies inside the timed region
+    if not args.no_e2e:
+        G_host = torch.empty(tot, dtype=gdt, pin_memory=True)
+        W_host = torch.empty(tot, dtype=wdt, pin_memory=True)
+        G_host.copy_(G_flat)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 5))
+        barrier(dist)
+        e0.record()
+        for _ in range(n_e2e):
+            for _ in range(wl.K):
+                G_flat.copy_(G_host, non_blocking=True)
+                opt_step(step_counter[0])
+                step_counter[0] += 1
+                W_host.copy_(W_flat, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / (n_e2e * wl.K), device)
+        line["e2e"] = {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": tot * gb,
+                       "d2h_bytes_per_step": tot * wb, "periods": n_e2e}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, detail = oracle_sample(wl)
+        line["cpu_baseline"] = {"value": round(v, 3), "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": (f"one matrix per shape group ({len(detail)} groups) through one K={wl.K} "
+                                           f"period, extrapolated by group counts to {len(shapes)} matrices"),
+                                "detail": detail}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    import torch
+    if args.impl == "reference":
+        run_reference(args, torch)
+    else:
+        run_ours(args, torch)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+/*
+ * muon.h -- C ABI of the GB300 (sm_103a) Muon / Periodic Row-wise Muon optimizer step.
+ *
+ * What the library computes (per 2-D weight matrix W of shape A x B, row-major):
+ *
+ *   momentum      M <- mu*M + G
+ *                 ("Muon is Scalable for LLM Training" notes, section 2.1, Eq. (1));
+ *   Newton-Schulz X0 = M/||M||_F, five times X <- a X + b (X X^T) X + c (X X^T)^2 X,
+ *                 (a, b, c) = (3.4445, -4.7750, 2.0315), run on the short side of M
+ *                 (same page, section 2.1, Eq. (2); section 2.2 for N = 5);
+ *   RowNorm       each of the min(A, B) lines of M along its long dimension scaled
+ *                 to unit L2 norm: rows when A <= B, columns when A > B
+ *                 ("Scaling Muon for Diffusion Transformers", abstract and the
+ *                 Periodic Row-wise / distributed-implementation paragraphs);
+ *   apply         W <- W - eta*(s*U + lambda*W) with s = 0.2*sqrt(max(A, B)) on NS5
+ *                 steps and gamma*0.2*sqrt(max(A, B)) on RowNorm steps
+ *                 ("Muon is Scalable" notes, Eq. (3), (4), (7));
+ *   schedule      NS5 refresh iff step % K == 0 (step counted from 0), RowNorm
+ *                 otherwise ("Scaling Muon for Diffusion Transformers", Periodic
+ *                 Row-wise paragraph; K = 1 is vanilla Muon).
+ *
+ * Conventions for every entry point:
+ *  - Memory: all tensor pointers are DEVICE pointers owned by the caller (for
+ *    example PyTorch allocations).  The library allocates no device memory and
+ *    frees nothing.  Scratch space comes from the caller's workspace `ws`
+ *    (device, 256-byte aligned, at least muon_workspace_size() bytes).  Arrays of
+ *    muon_matrix and arrays of output pointers are HOST arrays, read during the
+ *    call only.
+ *  - Layout: W, G, M, O and R are row-major A x B with leading dimension B (dense).
+ *    M is always fp32.  W and G are fp32 or bf16 (MUON_DTYPE_*); within one call
+ *    every matrix uses the same (w_dtype, g_dtype) pair.
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Every
+ *    call only enqueues work on it, never synchronises (except muon_check_status),
+ *    and is safe to capture into a CUDA graph.
+ *  - Errors: host-side validation happens before any launch; on error nothing is
+ *    enqueued and a negative muon_status is returned.  Device-side failures
+ *    (bounded waits that expired) are recorded in the workspace's status word and
+ *    read by muon_check_status().
+ *  - Matrices with A == 0 or B == 0 are accepted and skipped; n == 0 is a no-op.
+ *  - Determinism: all reductions use a fixed order, so identical inputs give
+ *    bit-identical outputs run to run.
+ */
+#ifndef MUON_GB300_MUON_H
+#define MUON_GB300_MUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MUON_ABI_VERSION 1
+
+typedef enum muon_status {
+  MUON_OK = 0,
+  MUON_ERR_INVALID = -1,     /* bad argument: null pointer, negative size, K < 1, step < 0 */
+  MUON_ERR_UNSUPPORTED = -2, /* dtype not supported, mixed dtypes, size beyond limits */
+  MUON_ERR_WORKSPACE = -3,   /* workspace null, misaligned or smaller than required */
+  MUON_ERR_CUDA = -4,        /* a CUDA runtime or driver call failed */
+  MUON_ERR_TIMEOUT = -5,     /* a device-side bounded wait expired (from muon_check_status) */
+  MUON_ERR_NO_DEVICE = -6    /* no usable sm_103 device is current */
+} muon_status;
+
+enum { MUON_DTYPE_F32 = 0, MUON_DTYPE_BF16 = 1 };
+
+/* Newton-Schulz arithmetic: bf16 operands with fp32 accumulation on the tensor
+ * cores (tcgen05), or fp32 throughout on the CUDA cores. */
+enum { MUON_NS5_BF16 = 0, MUON_NS5_F32 = 1 };
+
+/* Branch reported by muon_periodic_step. */
+enum { MUON_BRANCH_ROWNORM = 0, MUON_BRANCH_NS5 = 1 };
+
+typedef struct muon_matrix {
+  void* W;          /* device, A x B row-major, w_dtype; updated in place           */
+  const void* G;    /* device, A x B row-major, g_dtype; the step's gradient         */
+  float* M;         /* device, A x B row-major, fp32 momentum; updated in place      */
+  int64_t rows;     /* A (0 <= A < 2^31)                                             */
+  int64_t cols;     /* B (0 <= B < 2^31)                                             */
+  int32_t w_dtype;  /* MUON_DTYPE_F32 or MUON_DTYPE_BF16                             */
+  int32_t g_dtype;  /* MUON_DTYPE_F32 or MUON_DTYPE_BF16                             */
+} muon_matrix;
+
+typedef void* muon_stream_t; /* cudaStream_t */
+
+/* Bytes of workspace any entry point needs for this matrix list and NS5 mode
+ * (the maximum over all entry points; one workspace serves them all).
+ * Returns 0 for n == 0, and (size_t)-1 for an invalid list. */
+size_t muon_workspace_size(const muon_matrix* mats, int n, int ns5_mode);
+
+/* Momentum, Eq. (1) of the "Muon is Scalable" notes (section 2.1):
+ *   M_i <- mu*M_i + G_i for every matrix.
+ * fro_sq_out: optional device array of n floats; when non-NULL it receives
+ * ||M_i||_F^2 of the updated momentum (fixed-order fp32 reduction), and ws must
+ * be a valid workspace.  W is not read.  ws may be NULL when fro_sq_out is NULL. */
+int muon_momentum(const muon_matrix* mats, int n, float mu, float* fro_sq_out,
+                  void* ws, size_t ws_bytes, muon_stream_t stream);
+
+/* Frobenius norm of the current momentum, the normaliser of X0 = M/||M||_F
+ * (section 2.1 of the "Muon is Scalable" notes): fro_out[i] = ||M_i||_F (device,
+ * n floats).  M is read only; G and W are not read. */
+int muon_fro_norm(const muon_matrix* mats, int n, float* fro_out,
+                  void* ws, size_t ws_bytes, muon_stream_t stream);
+
+/* Newton-Schulz-5 of the current momentum, Eq. (2) of the "Muon is Scalable"
+ * notes: O_i = NS5(M_i), computed on the short side of M_i and returned in
+ * M_i's A x B orientation.  O_out: host array of n device pointers, each an
+ * A x B row-major buffer of o_dtype.  ns5_mode selects the arithmetic
+ * (MUON_NS5_BF16: bf16 tensor-core GEMMs, fp32 accumulate, bf16 intermediates;
+ * MUON_NS5_F32: fp32 throughout).  M, G and W are not modified.  A zero M gives
+ * O = 0. */
+int muon_ns5_batched(const muon_matrix* mats, int n, int ns5_mode, void* const* O_out,
+                     int o_dtype, void* ws, size_t ws_bytes, muon_stream_t stream);
+
+/* RowNorm of the current momentum (Periodic Row-wise branch): R_i = M_i with each
+ * row (A <= B) or each column (A > B) scaled to unit L2 norm; a zero line stays
+ * zero.  R_out: host array of n device pointers to fp32 A x B buffers.  M is
+ * read only. */
+int muon_rownorm(const muon_matrix* mats, int n, float* const* R_out,
+                 void* ws, size_t ws_bytes, muon_stream_t stream);
+
+/* Apply, Eq. (4)/(7) of the "Muon is Scalable" notes:
+ *   W_i <- W_i - eta*(scale_mul*sqrt(max(A, B))*U_i + lambda*W_i)
+ * computed in fp32 with one rounding to w_dtype.  U: host array of n device
+ * pointers to A x B buffers of u_dtype.  scale_mul is 0.2 for an NS5 direction
+ * and 0.2*gamma for a RowNorm direction. */
+int muon_apply(const muon_matrix* mats, int n, const void* const* U, int u_dtype,
+               float scale_mul, float eta, float lambda, muon_stream_t stream);
+
+/* One Periodic Row-wise Muon step over every matrix (K = 1: vanilla Muon):
+ *   refresh = (step % K == 0);
+ *   M <- mu*M + G;
+ *   U = NS5(M) (refresh) or RowNorm(M) (otherwise);
+ *   W <- W - eta*(s*U + lambda*W), s = 0.2*sqrt(max(A, B)), times gamma when not refreshing.
+ * On refresh steps the apply is fused into the last Newton-Schulz GEMM; on
+ * RowNorm steps momentum, normalisation and apply are one pass over memory for
+ * wide matrices and two passes for tall ones.  branch_out (host, optional)
+ * receives MUON_BRANCH_NS5 or MUON_BRANCH_ROWNORM. */
+int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, float gamma,
+                       float mu, float eta, float lambda, int ns5_mode, void* ws,
+                       size_t ws_bytes, muon_stream_t stream, int* branch_out);
+
+/* Clears the status header of a fresh workspace (the first 256 bytes) on
+ * `stream`.  Call once after allocating a workspace whose contents are not
+ * already zero; the rest of the workspace needs no initialisation. */
+int muon_workspace_init(void* ws, size_t ws_bytes, muon_stream_t stream);
+
+/* Synchronises `stream`, reads and clears the device status word in `ws`, and
+ * returns MUON_OK or the recorded error (MUON_ERR_TIMEOUT). */
+int muon_check_status(void* ws, size_t ws_bytes, muon_stream_t stream);
+
+/* Profiling hook (process-wide): up to 5 cudaEvent_t handles that
+ * muon_periodic_step records on its stream at phase boundaries:
+ *   [0] refresh step start, [1] first Newton-Schulz GEMM launch,
+ *   [2] after the last Newton-Schulz GEMM, [3] RowNorm step start,
+ *   [4] RowNorm step end.
+ * NULL entries are skipped; n == 0 turns the hook off.  Recording also works
+ * under stream capture (the records become graph nodes). */
+int muon_profile_events(void* const* events, int n);
+
+/* Number of kernels that the most recent entry-point call made by this host
+ * thread enqueued (0 after a validation error). */
+int muon_launch_count(void);
+
+/* Static description of a status code. */
+const char* muon_status_str(int status);
+
+/* MUON_ABI_VERSION of the loaded library. */
+int muon_abi_version(void);
+
+/* Test hooks (process-wide, not for production use).
+ * timeout_ms: limit of every device-side wait (default 4000 ms; 0 restores it).
+ * flags: MUON_DEBUG_STALL_PRODUCER makes the tensor-core GEMM's load warp issue
+ * nothing, so that its consumers' bounded waits expire and report
+ * MUON_ERR_TIMEOUT through muon_check_status (no fault, no hang). */
+enum { MUON_DEBUG_STALL_PRODUCER = 1 };
+int muon_debug_set(int flags, int timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MUON_GB300_MUON_H */

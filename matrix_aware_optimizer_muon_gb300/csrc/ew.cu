@@ -1,0 +1,478 @@
+// Bandwidth-bound kernels of the Muon step.
+//
+//  * ew_tile_kernel: one pass over 64 x 128 tiles of M (and G, W) doing any
+//    combination of: momentum M <- mu*M + G ("Muon is Scalable" notes, section
+//    2.1, Eq. (1)); per-tile sum of squares for ||M||_F (section 2.1, X0 = M/||M||_F);
+//    the bf16/fp32 copy X~ of M on the short-side orientation that feeds the
+//    Newton-Schulz GEMMs; per-tile line partial sums for RowNorm; and the second
+//    RowNorm pass W <- W - eta*(s*M/||line|| + lambda*W) (Eq. (4) with the
+//    Periodic Row-wise scale).
+//  * rows_kernel: the whole RowNorm step for a wide/square matrix in one pass:
+//    one CTA per row keeps the row in registers (momentum, row norm, apply).
+//  * apply_kernel: W <- W - eta*(s*U + lambda*W) from a given direction U.
+//  * fro_final_kernel / line_final_kernel: fixed-order reductions of partials.
+//
+// Every reduction has a fixed order, so results are bit-reproducible.
+#include "common.cuh"
+#include "internal.h"
+
+namespace muon {
+
+template <typename T, int N>
+struct alignas(16) Arr { T v[N]; };
+
+__device__ __forceinline__ int find_mat_ew(const EwParams& p, int t) {
+  int lo = 0, hi = p.nmat - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.mat[mid].tile_begin <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <typename WT, typename GT, typename XT, int MODE>
+__global__ void __launch_bounds__(EW_THREADS)
+ew_tile_kernel(const __grid_constant__ EwParams p) {
+  constexpr bool kMom = (MODE & EW_MOMENTUM) != 0;
+  constexpr bool kFro = (MODE & EW_FRO) != 0;
+  constexpr bool kXT = (MODE & EW_XT) != 0;
+  constexpr bool kLine = (MODE & EW_LINEPART) != 0;
+  constexpr bool kApply = (MODE & EW_APPLY_LINE) != 0;
+  constexpr bool kR = (MODE & EW_WRITE_R) != 0;
+  constexpr int RPT = TILE_R / (EW_THREADS / 32);  // rows per thread = 8
+
+  __shared__ float red[32];
+
+  const int t = blockIdx.x;
+  const int mi = find_mat_ew(p, t);
+  const EwMat& mt = p.mat[mi];
+  const int lt = t - mt.tile_begin;
+  const int tr = lt / mt.tiles_c;
+  const int tc = lt - tr * mt.tiles_c;
+  const int r0 = tr * TILE_R, c0 = tc * TILE_C;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = mt.rows, cols = mt.cols;
+  const int cb = c0 + lane * 4;
+  const bool vec = mt.vec && (cb + 4 <= cols);
+  float* __restrict__ Mp = mt.M;
+
+  float v[RPT][4];
+  float w[kApply ? RPT : 1][4];
+  float inv_col[4] = {0.f, 0.f, 0.f, 0.f};
+  if constexpr (kApply || kR) {
+    if (mt.tall) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) inv_col[j] = (cb + j < cols) ? mt.line_inv[cb + j] : 0.f;
+    }
+  }
+
+  // ---- load (and momentum) ----
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = r0 + warp + (EW_THREADS / 32) * i;
+    const bool rok = r < rows;
+    const size_t off = (size_t)r * (size_t)cols + (size_t)cb;
+    if (rok && vec) {
+      ld4(Mp + off, v[i]);
+      if constexpr (kMom) {
+        float g[4];
+        ld4_stream(reinterpret_cast<const GT*>(mt.G) + off, g);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[i][j] = p.mu * v[i][j] + g[j];
+      }
+      if constexpr (kApply) ld4(reinterpret_cast<const WT*>(mt.W) + off, w[i]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool ok = rok && (cb + j < cols);
+        float m = ok ? Mp[off + j] : 0.f;
+        if constexpr (kMom) {
+          if (ok) m = p.mu * m + ld1(reinterpret_cast<const GT*>(mt.G) + off + j);
+        }
+        v[i][j] = m;
+        if constexpr (kApply) w[i][j] = ok ? ld1(reinterpret_cast<const WT*>(mt.W) + off + j) : 0.f;
+      }
+    }
+  }
+
+  // ---- store momentum ----
+  if constexpr (kMom) {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int r = r0 + warp + (EW_THREADS / 32) * i;
+      if (r >= rows) continue;
+      const size_t off = (size_t)r * (size_t)cols + (size_t)cb;
+      if (vec) {
+        st4(Mp + off, v[i]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (cb + j < cols) Mp[off + j] = v[i][j];
+      }
+    }
+  }
+
+  // ---- per-tile sum of squares (Frobenius partial) ----
+  if constexpr (kFro) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ss = fmaf(v[i][j], v[i][j], ss);
+    ss = block_sum(ss, red);
+    if (threadIdx.x == 0) mt.part[lt] = ss;
+  }
+
+  // ---- line partials ----
+  if constexpr (kLine) {
+    if (mt.tall) {
+      // columns are the lines: sum over this tile's 64 rows, fixed order
+      __shared__ float colred[EW_THREADS / 32][TILE_C];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) s = fmaf(v[i][j], v[i][j], s);
+        colred[warp][lane * 4 + j] = s;
+      }
+      __syncthreads();
+      if (threadIdx.x < TILE_C) {
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < EW_THREADS / 32; ++k) s += colred[k][threadIdx.x];
+        const int c = c0 + threadIdx.x;
+        if (c < cols) mt.line_part[(size_t)tr * cols + c] = s;
+      }
+    } else {
+      // rows are the lines: sum over this tile's 128 columns
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s = fmaf(v[i][j], v[i][j], s);
+        s = warp_sum(s);
+        const int r = r0 + warp + (EW_THREADS / 32) * i;
+        if (lane == 0 && r < rows) mt.line_part[(size_t)tc * rows + r] = s;
+      }
+    }
+  }
+
+  // ---- RowNorm output or apply ----
+  if constexpr (kApply || kR) {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int r = r0 + warp + (EW_THREADS / 32) * i;
+      if (r >= rows) continue;
+      const float inv_row = mt.tall ? 0.f : mt.line_inv[r];
+      float u[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) u[j] = v[i][j] * (mt.tall ? inv_col[j] : inv_row);
+      const size_t off = (size_t)r * (size_t)cols + (size_t)cb;
+      if constexpr (kR) {
+        float* R = reinterpret_cast<float*>(mt.aux);
+        if (vec) st4(R + off, u);
+        else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) if (cb + j < cols) R[off + j] = u[j];
+        }
+      }
+      if constexpr (kApply) {
+        float o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = w[i][j] - p.eta * (mt.scale * u[j] + p.lam * w[i][j]);
+        WT* Wp = reinterpret_cast<WT*>(mt.W);
+        if (vec) st4(Wp + off, o);
+        else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) if (cb + j < cols) st1(Wp + off + j, o[j]);
+        }
+      }
+    }
+  }
+
+  // ---- X~ on the short-side orientation ----
+  if constexpr (kXT) {
+    XT* X = reinterpret_cast<XT*>(mt.aux);
+    const int ld = mt.ld_aux;
+    if (!mt.tall) {
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int r = r0 + warp + (EW_THREADS / 32) * i;
+        if (r >= rows) continue;
+        const size_t off = (size_t)r * ld + cb;
+        if (cb + 4 <= cols) st4(X + off, v[i]);
+        else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) if (cb + j < cols) st1(X + off + j, v[i][j]);
+        }
+      }
+    } else {
+      // X~ = M^T: stage the tile transposed in shared memory, then write rows of X~.
+      constexpr int PAD = 2;
+      __shared__ XT tb[TILE_C][TILE_R + PAD];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int rl = warp + (EW_THREADS / 32) * i;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tb[lane * 4 + j][rl] = from_f32<XT>(v[i][j]);
+      }
+      __syncthreads();
+      const int rr = r0 + 2 * lane;  // this lane's two M rows = two X~ columns
+#pragma unroll 4
+      for (int k = 0; k < TILE_C / (EW_THREADS / 32); ++k) {
+        const int cl = warp + (EW_THREADS / 32) * k;
+        const int c = c0 + cl;
+        if (c >= cols) continue;
+        XT* dst = X + (size_t)c * ld + rr;
+        if (rr + 1 < rows) {
+          dst[0] = tb[cl][2 * lane];
+          dst[1] = tb[cl][2 * lane + 1];
+        } else if (rr < rows) {
+          dst[0] = tb[cl][2 * lane];
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// single-pass RowNorm step, rows of a wide/square matrix
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int find_mat_rows(const RowsParams& p, int t) {
+  int lo = 0, hi = p.nmat - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.mat[mid].row_begin <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <typename WT, typename GT, int CPT>
+__global__ void __launch_bounds__(512)
+rows_kernel(const __grid_constant__ RowsParams p) {
+  __shared__ float red[32];
+  const int rg = blockIdx.x;
+  const RowsMat& mt = p.mat[find_mat_rows(p, rg)];
+  const int r = rg - mt.row_begin;
+  const int cols = mt.cols;
+  const size_t base = (size_t)r * (size_t)cols;
+  float* __restrict__ Mp = mt.M + base;
+  const GT* __restrict__ Gp = reinterpret_cast<const GT*>(mt.G) + base;
+  WT* __restrict__ Wp = reinterpret_cast<WT*>(mt.W) + base;
+
+  float v[CPT][4], w[CPT][4];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) {
+    const int c = (threadIdx.x + k * blockDim.x) * 4;
+    if (mt.vec && c + 4 <= cols) {
+      float g[4];
+      ld4(Mp + c, v[k]);
+      ld4_stream(Gp + c, g);
+      ld4(Wp + c, w[k]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[k][j] = p.mu * v[k][j] + g[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool ok = c + j < cols;
+        v[k][j] = ok ? p.mu * Mp[c + j] + ld1(Gp + c + j) : 0.f;
+        w[k][j] = ok ? ld1(Wp + c + j) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ss = fmaf(v[k][j], v[k][j], ss);
+  }
+  const float inv = inv_norm_from_sumsq(block_sum(ss, red));
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) {
+    const int c = (threadIdx.x + k * blockDim.x) * 4;
+    float o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = w[k][j] - p.eta * (mt.scale * (v[k][j] * inv) + p.lam * w[k][j]);
+    if (mt.vec && c + 4 <= cols) {
+      st4(Mp + c, v[k]);
+      st4(Wp + c, o);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (c + j < cols) { Mp[c + j] = v[k][j]; st1(Wp + c + j, o[j]); }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// apply from a given direction
+// ---------------------------------------------------------------------------
+template <typename WT, typename UT>
+__global__ void __launch_bounds__(256)
+apply_kernel(const __grid_constant__ ApplyParams p) {
+  int lo = 0, hi = p.nmat - 1;
+  const int b = blockIdx.x;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.mat[mid].block_begin <= b) lo = mid; else hi = mid - 1;
+  }
+  const ApplyMat& mt = p.mat[lo];
+  const long long e0 = (long long)(b - mt.block_begin) * APPLY_CHUNK;
+  WT* Wp = reinterpret_cast<WT*>(mt.W);
+  const UT* Up = reinterpret_cast<const UT*>(mt.U);
+#pragma unroll
+  for (int k = 0; k < APPLY_CHUNK / (256 * 4); ++k) {
+    const long long e = e0 + (long long)(k * 256 + threadIdx.x) * 4;
+    if (mt.vec && e + 4 <= mt.numel) {
+      float w[4], u[4], o[4];
+      ld4(Wp + e, w);
+      ld4_stream(Up + e, u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = w[j] - p.eta * (mt.scale * u[j] + p.lam * w[j]);
+      st4(Wp + e, o);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (e + j < mt.numel) {
+          const float w = ld1(Wp + e + j), u = ld1(Up + e + j);
+          st1(Wp + e + j, w - p.eta * (mt.scale * u + p.lam * w));
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// fixed-order finalisers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ double block_sum_f64(double v, double* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  double t = 0.0;
+  if (warp == 0) {
+    t = (lane < (int)(blockDim.x >> 5)) ? red[lane] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  }
+  return t;
+}
+
+// One CTA per matrix: ||M_i||^2 = sum of the matrix's tile partials (fixed order).
+__global__ void __launch_bounds__(256)
+fro_final_kernel(const __grid_constant__ FroFinalParams p) {
+  __shared__ double red[32];
+  const int i = blockIdx.x;
+  const int b = p.begin[i], e = p.begin[i] + p.count[i];
+  double s = 0.0;
+  for (int t = b + threadIdx.x; t < e; t += blockDim.x) s += (double)p.part[t];
+  s = block_sum_f64(s, red);
+  if (threadIdx.x == 0) {
+    const int o = p.out_index[i];
+    const float ss = (float)s;
+    if (p.fro_sq) p.fro_sq[o] = ss;
+    if (p.inv_norm) p.inv_norm[o] = inv_norm_from_sumsq(ss);
+    if (p.fro) p.fro[o] = sqrtf(ss);
+  }
+}
+
+// One thread per line: inv[l] = 1/sqrt(sum over the partial rows), fixed order.
+__global__ void __launch_bounds__(256)
+line_final_kernel(const __grid_constant__ LineFinalParams p) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= p.total_lines) return;
+  int lo = 0, hi = p.nmat - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.mat[mid].line_begin <= g) lo = mid; else hi = mid - 1;
+  }
+  const LineFinalMat& mt = p.mat[lo];
+  const int l = g - mt.line_begin;
+  double s = 0.0;
+  for (int q = 0; q < mt.parts; ++q) s += (double)mt.part[(size_t)q * mt.lines + l];
+  mt.inv[l] = inv_norm_from_sumsq((float)s);
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+template <typename WT, typename GT, typename XT>
+static cudaError_t launch_ew_t(int mode, const EwParams& p, cudaStream_t s) {
+  const dim3 grid(p.total_tiles), block(EW_THREADS);
+  switch (mode) {
+#define MUON_EW_CASE(M) \
+  case (M): ew_tile_kernel<WT, GT, XT, (M)><<<grid, block, 0, s>>>(p); break;
+    MUON_EW_CASE(EW_MOMENTUM)
+    MUON_EW_CASE(EW_MOMENTUM | EW_FRO)
+    MUON_EW_CASE(EW_MOMENTUM | EW_FRO | EW_XT)
+    MUON_EW_CASE(EW_FRO | EW_XT)
+    MUON_EW_CASE(EW_FRO)
+    MUON_EW_CASE(EW_MOMENTUM | EW_LINEPART)
+    MUON_EW_CASE(EW_LINEPART)
+    MUON_EW_CASE(EW_APPLY_LINE)
+    MUON_EW_CASE(EW_WRITE_R)
+#undef MUON_EW_CASE
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ew(int mode, int w_dt, int g_dt, int x_dt, const EwParams& p, cudaStream_t s) {
+  if (p.total_tiles <= 0) return cudaSuccess;
+  const bool wb = w_dt == MUON_DTYPE_BF16, gb = g_dt == MUON_DTYPE_BF16, xb = x_dt == MUON_DTYPE_BF16;
+  if (wb && gb) return xb ? launch_ew_t<bf16, bf16, bf16>(mode, p, s) : launch_ew_t<bf16, bf16, float>(mode, p, s);
+  if (wb && !gb) return xb ? launch_ew_t<bf16, float, bf16>(mode, p, s) : launch_ew_t<bf16, float, float>(mode, p, s);
+  if (!wb && gb) return xb ? launch_ew_t<float, bf16, bf16>(mode, p, s) : launch_ew_t<float, bf16, float>(mode, p, s);
+  return xb ? launch_ew_t<float, float, bf16>(mode, p, s) : launch_ew_t<float, float, float>(mode, p, s);
+}
+
+template <typename WT, typename GT>
+static cudaError_t launch_rows_t(int max_cols, const RowsParams& p, cudaStream_t s) {
+  const int chunks = (max_cols + 3) / 4;
+  const int T = chunks <= 128 * 8 ? 128 : (chunks <= 256 * 8 ? 256 : 512);
+  const int cpt = (chunks + T - 1) / T;
+  const dim3 grid(p.total_rows), block(T);
+  switch (cpt) {
+#define MUON_ROWS_CASE(C) \
+  case (C): rows_kernel<WT, GT, (C)><<<grid, block, 0, s>>>(p); break;
+    MUON_ROWS_CASE(1) MUON_ROWS_CASE(2) MUON_ROWS_CASE(3) MUON_ROWS_CASE(4)
+    MUON_ROWS_CASE(5) MUON_ROWS_CASE(6) MUON_ROWS_CASE(7) MUON_ROWS_CASE(8)
+#undef MUON_ROWS_CASE
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows(int w_dt, int g_dt, int max_cols, const RowsParams& p, cudaStream_t s) {
+  if (p.total_rows <= 0) return cudaSuccess;
+  if (max_cols > ROWS_MAX_COLS) return cudaErrorInvalidValue;
+  const bool wb = w_dt == MUON_DTYPE_BF16, gb = g_dt == MUON_DTYPE_BF16;
+  if (wb && gb) return launch_rows_t<bf16, bf16>(max_cols, p, s);
+  if (wb && !gb) return launch_rows_t<bf16, float>(max_cols, p, s);
+  if (!wb && gb) return launch_rows_t<float, bf16>(max_cols, p, s);
+  return launch_rows_t<float, float>(max_cols, p, s);
+}
+
+cudaError_t launch_apply(int w_dt, int u_dt, const ApplyParams& p, cudaStream_t s) {
+  if (p.total_blocks <= 0) return cudaSuccess;
+  const dim3 grid(p.total_blocks), block(256);
+  const bool wb = w_dt == MUON_DTYPE_BF16, ub = u_dt == MUON_DTYPE_BF16;
+  if (wb && ub) apply_kernel<bf16, bf16><<<grid, block, 0, s>>>(p);
+  else if (wb && !ub) apply_kernel<bf16, float><<<grid, block, 0, s>>>(p);
+  else if (!wb && ub) apply_kernel<float, bf16><<<grid, block, 0, s>>>(p);
+  else apply_kernel<float, float><<<grid, block, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fro_final(const FroFinalParams& p, cudaStream_t s) {
+  if (p.nmat <= 0) return cudaSuccess;
+  fro_final_kernel<<<p.nmat, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_line_final(const LineFinalParams& p, cudaStream_t s) {
+  if (p.total_lines <= 0) return cudaSuccess;
+  line_final_kernel<<<(p.total_lines + 255) / 256, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace muon

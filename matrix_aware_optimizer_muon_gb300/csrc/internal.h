@@ -1,0 +1,237 @@
+// Internal declarations: launch-parameter tables, the workspace plan, and the
+// launchers each kernel file provides to the C ABI layer (api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/muon.h"
+
+namespace muon {
+
+// ---------------------------------------------------------------------------
+// element-wise tile kernels (64 x 128 tiles of the A x B matrix)
+// ---------------------------------------------------------------------------
+constexpr int TILE_R = 64;
+constexpr int TILE_C = 128;
+constexpr int EW_THREADS = 256;
+constexpr int EW_MAX_MATS = 96;  // matrices per launch (kernel-parameter table)
+
+enum EwMode : int {
+  EW_MOMENTUM = 1,   // M <- mu*M + G (stored)
+  EW_FRO = 2,        // per-tile sum of squares of M -> part[tile]
+  EW_XT = 4,         // X~ = M on the short-side orientation -> aux (ld_aux)
+  EW_LINEPART = 8,   // per-tile line partial sums of squares -> line_part
+  EW_APPLY_LINE = 16,// W <- W - eta*(s*M*inv_line + lambda*W)
+  EW_WRITE_R = 32,   // R = M*inv_line -> aux (fp32, ld = B)
+};
+
+struct EwMat {
+  void* W;
+  const void* G;
+  float* M;
+  void* aux;               // X~ (EW_XT) or R (EW_WRITE_R)
+  float* part;             // per-tile partials of this matrix (EW_FRO)
+  float* line_part;        // [tiles along the long dim][lines] (EW_LINEPART)
+  const float* line_inv;   // [lines] (EW_APPLY_LINE / EW_WRITE_R)
+  int rows, cols;
+  int ld_aux;
+  int tiles_c;             // ceil(cols / TILE_C)
+  int tile_begin;          // first tile of this matrix in the launch
+  int tall;                // rows > cols
+  float scale;             // apply scale s (already includes gamma)
+  int vec;                 // 4-wide vector path allowed
+};
+
+struct EwParams {
+  EwMat mat[EW_MAX_MATS];
+  int nmat;
+  int total_tiles;
+  float mu, eta, lam;
+};
+
+// single-pass RowNorm step for wide / square matrices (one CTA per row)
+constexpr int ROWS_MAX_MATS = 128;
+constexpr int ROWS_MAX_COLS = 16384;
+
+struct RowsMat {
+  void* W;
+  const void* G;
+  float* M;
+  int rows, cols;
+  int row_begin;
+  float scale;
+  int vec;
+};
+struct RowsParams {
+  RowsMat mat[ROWS_MAX_MATS];
+  int nmat;
+  int total_rows;
+  float mu, eta, lam;
+};
+
+// apply from a given direction U
+constexpr int APPLY_MAX_MATS = 128;
+constexpr int APPLY_CHUNK = 4096;  // elements per CTA
+struct ApplyMat {
+  void* W;
+  const void* U;
+  int64_t numel;
+  int block_begin;
+  float scale;
+  int vec;
+};
+struct ApplyParams {
+  ApplyMat mat[APPLY_MAX_MATS];
+  int nmat;
+  int total_blocks;
+  float eta, lam;
+};
+
+// fixed-order finalisers
+constexpr int FIN_MAX_MATS = 512;
+struct FroFinalParams {
+  const float* part;          // tile partials
+  int begin[FIN_MAX_MATS];    // first partial of matrix i
+  int count[FIN_MAX_MATS];    // number of partials of matrix i
+  int out_index[FIN_MAX_MATS];// output slot of matrix i
+  int nmat;
+  float* fro_sq;              // optional outputs, indexed by out_index
+  float* inv_norm;
+  float* fro;
+};
+constexpr int LINE_MAX_MATS = 256;
+struct LineFinalMat {
+  const float* part;          // [parts][lines]
+  float* inv;                 // [lines]
+  int parts, lines, line_begin;
+};
+struct LineFinalParams {
+  LineFinalMat mat[LINE_MAX_MATS];
+  int nmat;
+  int total_lines;
+};
+
+// ---------------------------------------------------------------------------
+// Newton-Schulz GEMMs
+// ---------------------------------------------------------------------------
+enum GemmKind : int { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_UPDATE = 2 };
+enum NsFlags : int { NS_TALL = 1, NS_MVEC = 2 };
+// Iterations 1..NS_LO_ITERS add a bf16 residual to the bf16 X in the a*X term
+// (X carried with ~16 significant bits where the small singular directions are
+// still far below the element magnitudes).
+constexpr int NS_LO_ITERS = 2;
+
+constexpr int NS_MAX_GROUPS = 8;
+constexpr int NS_MAX_MATS = 512;
+
+// One shape group (same short side n and long side m) inside one GEMM launch.
+struct NsGroup {
+  CUtensorMap mapA;        // tensor-core path: K-major A operand
+  CUtensorMap mapB;        // tensor-core path: B operand (K-major or MN-major)
+  const void* opA;         // SIMT path: A operand base
+  const void* opB;         // SIMT path: B operand base
+  const void* epi_in;      // POLY: S (b*S term); UPDATE: X_in (a*X term)
+  void* out;               // GRAM: S; POLY: B; UPDATE: X_out
+  const void* lo_in;       // UPDATE (tensor-core path): bf16 residual of X_in, or null
+  void* lo_out;            // UPDATE (tensor-core path): bf16 residual of X_out, or null
+  long long stride_nn;     // elements between matrices of an n x n buffer
+  long long stride_nm;     // elements between matrices of an n x m buffer
+  int ld_n, ld_m;          // leading dims of n x n and n x m buffers
+  int n, m;
+  int count;
+  int mtiles, ntiles;      // output tiles (rows, cols)
+  int tiles_per_mat;
+  int tile_begin;
+  int mat_base;            // index of the group's first matrix in the launch tables
+};
+
+struct NsParams {
+  NsGroup g[NS_MAX_GROUPS];
+  int ngroups;
+  int total_tiles;
+  int kind;
+  float a, b, c;
+  int first_iter;          // fold 1/||M|| (UPDATE) or 1/||M||^2 (GRAM)
+  int last_iter;           // UPDATE: write O or apply to W instead of X_out
+  const float* inv_norm;   // per matrix (launch table order)
+  // last-iteration outputs, per matrix (launch table order)
+  void* dst[NS_MAX_MATS];  // W (apply) or O (output)
+  const float* msrc[NS_MAX_MATS];  // fp32 momentum, the exact X0 for the first a*X term
+  unsigned char flags[NS_MAX_MATS];  // NS_TALL | NS_MVEC
+  int dst_mode;            // 0: O in dst_dtype; 1: apply to W of dst_dtype
+  int dst_dtype;           // MUON_DTYPE_*
+  float eta, lam, rms_match;
+  unsigned int* status;    // device status word
+  unsigned long long timeout_ns;
+  int debug_flags;
+};
+
+// ---------------------------------------------------------------------------
+// workspace plan (identical for every entry point given the same matrix list)
+// ---------------------------------------------------------------------------
+struct MatPlan {
+  int A, B;
+  int n, m;                // short / long side
+  int tall;
+  int group;
+  int idx_in_group;
+  int tiles;               // 64 x 128 tiles
+  size_t fro_part;         // float offset of this matrix's tile partials
+  size_t line_part;        // float offset of line partials
+  size_t line_inv;         // float offset of inverse line norms
+  int line_tiles;          // number of partial rows (tiles along the long dim)
+  int lines;               // n
+};
+
+struct GroupPlan {
+  int n, m;
+  int count;
+  std::vector<int> mats;   // indices into the matrix list
+  int ld_n, ld_m;
+  size_t x0, x1, s, bm;    // byte offsets in the workspace
+  size_t lo0, lo1;         // bf16 residual ping-pong (tensor-core mode only)
+};
+
+struct Plan {
+  std::vector<MatPlan> mats;
+  std::vector<GroupPlan> groups;
+  int ns5_mode;
+  size_t status;           // byte offset of the status word (always 0)
+  size_t fro_part;         // byte offset of the fp32 tile-partial area
+  size_t fro_sq;           // per matrix ||M||^2
+  size_t inv_norm;         // per matrix 1/||M||
+  size_t line_part;
+  size_t line_inv;
+  size_t total;
+};
+
+// launchers (return a cudaError_t from the launch)
+cudaError_t launch_ew(int mode, int w_dt, int g_dt, int x_dt, const EwParams& p, cudaStream_t s);
+cudaError_t launch_rows(int w_dt, int g_dt, int max_cols, const RowsParams& p, cudaStream_t s);
+cudaError_t launch_apply(int w_dt, int u_dt, const ApplyParams& p, cudaStream_t s);
+cudaError_t launch_fro_final(const FroFinalParams& p, cudaStream_t s);
+cudaError_t launch_line_final(const LineFinalParams& p, cudaStream_t s);
+cudaError_t launch_ns_simt(const NsParams& p, cudaStream_t s);
+cudaError_t launch_ns_tc(const NsParams& p, cudaStream_t s, int num_sms);
+int ns_tc_smem_bytes();
+
+// tensor map encoding (driver entry point obtained through the runtime)
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1);
+
+}  // namespace muon
+
+namespace muon {
+// Kernel parameters are limited to 32764 bytes.
+static_assert(sizeof(EwParams) < 32000, "EwParams too large");
+static_assert(sizeof(RowsParams) < 32000, "RowsParams too large");
+static_assert(sizeof(ApplyParams) < 32000, "ApplyParams too large");
+static_assert(sizeof(FroFinalParams) < 32000, "FroFinalParams too large");
+static_assert(sizeof(LineFinalParams) < 32000, "LineFinalParams too large");
+static_assert(sizeof(NsParams) < 32000, "NsParams too large");
+}  // namespace muon

@@ -1,0 +1,444 @@
+// Newton-Schulz-5 GEMMs on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// One iteration of Eq. (2) of the "Muon is Scalable for LLM Training" notes
+// (section 2.1), X <- a X + b (X X^T) X + c (X X^T)^2 X, is computed in the
+// factored form
+//     S = X X^T               (GEMM_GRAM,   n x n, symmetric: upper tiles only)
+//     B = b S + c S S         (GEMM_POLY,   n x n, symmetric: upper tiles only)
+//     X <- a X + B X          (GEMM_UPDATE, n x m)
+// with bf16 operands, fp32 accumulation in tensor memory, and every output
+// rounded to bf16.  The first iteration folds X0 = M/||M||_F into the epilogues
+// (S scaled by 1/||M||^2, X by 1/||M||), so the momentum is never normalised in
+// a separate pass.  In the last iteration the UPDATE epilogue either writes O or
+// applies W <- W - eta*(0.2*sqrt(max(A, B))*O + lambda*W) (Eq. (4)/(7)) directly.
+//
+// Kernel shape: persistent, one CTA per SM, 192 threads.
+//   warp 0      TMA producer (one lane): 4-stage ring of 128x64 A and 256x64 B
+//               bf16 tiles, 128-byte swizzle;
+//   warp 1      TMEM allocator and MMA issuer (one lane): tcgen05.mma
+//               cta_group::1, M=128, N=256, K=16, two 256-column fp32
+//               accumulators so the epilogue of tile i overlaps the MMAs of i+1;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, fused combine,
+//               global stores (symmetric outputs are written with their mirror).
+// Tiles of all same-shape matrices (and of several shape groups) form one flat
+// list that CTAs walk with stride gridDim.x.  Every mbarrier wait is bounded in
+// time; on expiry the kernel records MUON_DEV_TIMEOUT in the status word, all
+// roles stop, in-flight copies and MMAs are drained (again bounded) and TMEM is
+// freed before exit.
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "ns_common.cuh"
+
+namespace muon {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 4;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr uint32_t DEV_TIMEOUT = 1u;
+
+struct Tile {
+  int g, mat, tm, tn;
+};
+
+__device__ __forceinline__ Tile decode(const NsParams& p, int t) {
+  Tile ti;
+  int g = 0;
+  while (g + 1 < p.ngroups && p.g[g + 1].tile_begin <= t) ++g;
+  const NsGroup& G = p.g[g];
+  int lt = t - G.tile_begin;
+  ti.g = g;
+  ti.mat = lt / G.tiles_per_mat;
+  int r = lt - ti.mat * G.tiles_per_mat;
+  if (p.kind == GEMM_UPDATE) {
+    ti.tn = r / G.mtiles;
+    ti.tm = r - ti.tn * G.mtiles;
+  } else {
+    // upper-triangle tiles of the n x n output: column block tn holds row
+    // blocks 0 .. min(2*tn+1, mtiles-1)
+    int tn = 0;
+    while (true) {
+      const int cnt = min(2 * tn + 2, G.mtiles);
+      if (r < cnt) break;
+      r -= cnt;
+      ++tn;
+    }
+    ti.tn = tn;
+    ti.tm = r;
+  }
+  return ti;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false on timeout (recorded in the
+// status word and the CTA's abort flag) or, when honor_abort, if another role
+// already aborted.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             const NsParams& p, bool honor_abort) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (honor_abort && *abort_flag) return false;
+    if (ptx::globaltimer() - t0 > p.timeout_ns) {
+      *abort_flag = 1;
+      if (p.status) atomicOr(p.status, DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(bf16* dst, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    reinterpret_cast<uint4*>(dst)[q] = u;
+  }
+}
+__device__ __forceinline__ void load_bf16x32(const bf16* src, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = reinterpret_cast<const uint4*>(src)[q];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[8 * q + 2 * h] = __uint_as_float(w[h] << 16);
+      v[8 * q + 2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
+    }
+  }
+}
+
+// Epilogue for 32 consecutive columns [c0, c0+32) of row r of one tile.
+__device__ __forceinline__ void epilogue_chunk(const NsParams& p, const NsGroup& G, const Tile& ti, int r,
+                                               int c0, float (&v)[32]) {
+  const int n = G.n, m = G.m;
+  const int gm = G.mat_base + ti.mat;
+  if (p.kind == GEMM_UPDATE) {
+    if (r >= n || c0 >= m) return;
+    const float sc = p.first_iter ? p.inv_norm[gm] : 1.0f;
+    const bool full = c0 + 32 <= m;
+    float x[32];
+    if (p.first_iter) {
+      // a*X0 from the fp32 momentum itself (X0 = M on the short side)
+      const float* Mp = p.msrc[gm];
+      if (p.flags[gm] & NS_TALL) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = (c0 + j < m) ? Mp[(size_t)(c0 + j) * n + r] : 0.f;
+      } else if (full && (p.flags[gm] & NS_MVEC)) {
+        const float4* src = reinterpret_cast<const float4*>(Mp + (size_t)r * m + c0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 f = src[q];
+          x[4 * q] = f.x; x[4 * q + 1] = f.y; x[4 * q + 2] = f.z; x[4 * q + 3] = f.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = (c0 + j < m) ? Mp[(size_t)r * m + c0 + j] : 0.f;
+      }
+    } else {
+      const bf16* Xin = reinterpret_cast<const bf16*>(G.epi_in) + (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m;
+      if (full) {
+        load_bf16x32(Xin + c0, x);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = (c0 + j < m) ? __bfloat162float(Xin[c0 + j]) : 0.f;
+      }
+      if (G.lo_in) {
+        const bf16* Lin = reinterpret_cast<const bf16*>(G.lo_in) + (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m;
+        float l[32];
+        if (full) {
+          load_bf16x32(Lin + c0, l);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) l[j] = (c0 + j < m) ? __bfloat162float(Lin[c0 + j]) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] += l[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = sc * (p.a * x[j] + v[j]);
+    if (!p.last_iter) {
+      const size_t off = (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m + c0;
+      bf16* Xout = reinterpret_cast<bf16*>(G.out) + off;
+      bf16* Lout = G.lo_out ? reinterpret_cast<bf16*>(G.lo_out) + off : nullptr;
+      float lo[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) lo[j] = v[j] - __bfloat162float(__float2bfloat16_rn(v[j]));
+      if (full) {
+        store_bf16x32(Xout, v);
+        if (Lout) store_bf16x32(Lout, lo);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < m) {
+            Xout[j] = __float2bfloat16_rn(v[j]);
+            if (Lout) Lout[j] = __float2bfloat16_rn(lo[j]);
+          }
+      }
+    } else {
+      const float s_apply = p.rms_match * sqrtf((float)m);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < m) ns_last_store(p, gm, n, m, r, c0 + j, v[j], s_apply);
+    }
+    return;
+  }
+
+  // symmetric n x n outputs: element (r, c) with r <= c is written at (r, c) and (c, r)
+  if (r >= n || c0 >= n) return;
+  if (r > c0 + 31) return;  // whole chunk below the diagonal
+  if (p.kind == GEMM_GRAM) {
+    const float sc = p.first_iter ? p.inv_norm[gm] * p.inv_norm[gm] : 1.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= sc;
+  } else {
+    const bf16* S = reinterpret_cast<const bf16*>(G.epi_in) + (size_t)ti.mat * G.stride_nn + (size_t)r * G.ld_n;
+    float s[32];
+    if (c0 + 32 <= n) {
+      load_bf16x32(S + c0, s);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) s[j] = (c0 + j < n) ? __bfloat162float(S[c0 + j]) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = p.b * s[j] + p.c * v[j];
+  }
+  bf16* out = reinterpret_cast<bf16*>(G.out) + (size_t)ti.mat * G.stride_nn;
+  if (r <= c0 && c0 + 32 <= n) {
+    store_bf16x32(out + (size_t)r * G.ld_n + c0, v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) out[(size_t)(c0 + j) * G.ld_n + r] = __float2bfloat16_rn(v[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int c = c0 + j;
+      if (c < n && r <= c) {
+        const bf16 h = __float2bfloat16_rn(v[j]);
+        out[(size_t)r * G.ld_n + c] = h;
+        out[(size_t)c * G.ld_n + r] = h;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_constant__ NsParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mdone = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], NUM_EPI_WARPS);
+    }
+    ptx::mbar_init(mdone, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  const int kind = p.kind;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && !(p.debug_flags & MUON_DEBUG_STALL_PRODUCER)) {
+      for (int g = 0; g < p.ngroups; ++g) {
+        ptx::prefetch_tmap(&p.g[g].mapA);
+        ptx::prefetch_tmap(&p.g[g].mapB);
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t pending = 0, pend_phase = 0;  // bit s: stage s has an issued load
+      bool stop = false;
+      for (int t = blockIdx.x; t < p.total_tiles && !stop; t += gridDim.x) {
+        const Tile ti = decode(p, t);
+        const NsGroup& G = p.g[ti.g];
+        const int K = (kind == GEMM_GRAM) ? G.m : G.n;
+        const int nkb = (K + BK - 1) / BK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p, true)) { stop = true; break; }
+          ptx::mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          const uint32_t sa = ptx::smem_addr(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          const int k0 = kb * BK;
+          ptx::tma_load_3d(sa, &G.mapA, &full[stage], k0, ti.tm * BM, ti.mat);
+          if (kind == GEMM_UPDATE) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              ptx::tma_load_3d(sb + j * (64 * BK * 2), &G.mapB, &full[stage], ti.tn * BN + 64 * j, k0, ti.mat);
+          } else {
+            ptx::tma_load_3d(sb, &G.mapB, &full[stage], k0, ti.tn * BN, ti.mat);
+          }
+          pending |= 1u << stage;
+          pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // drain: every issued copy must land before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if (pending & (1u << s)) wait_bounded(&full[s], (pend_phase >> s) & 1u, abort_flag, p, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, false, kind == GEMM_UPDATE);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool stop = false;
+      for (int t = blockIdx.x; t < p.total_tiles && !stop; t += gridDim.x, ++it) {
+        const Tile ti = decode(p, t);
+        const NsGroup& G = p.g[ti.g];
+        const int K = (kind == GEMM_GRAM) ? G.m : G.n;
+        const int nkb = (K + BK - 1) / BK;
+        const int acc = it & 1;
+        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, p, true)) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&full[stage], phase, abort_flag, p, true)) { stop = true; break; }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_addr(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; K step = 32 B.
+            const uint64_t adesc = ptx::smem_desc_sw128(sa + k * 32, 16, 1024);
+            // B: K-major like A (GRAM/POLY), or MN-major (UPDATE): 64-column
+            // atoms 8 KB apart (LBO), 8-row K groups 1024 B apart (SBO), K step = 16 rows.
+            const uint64_t bdesc = (kind == GEMM_UPDATE) ? ptx::smem_desc_sw128(sb + k * 2048, 64 * BK * 2, 1024)
+                                                         : ptx::smem_desc_sw128(sb + k * 32, 16, 1024);
+            ptx::mma_bf16(d, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(&empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (stop) break;
+        ptx::mma_commit(&tfull[acc]);
+      }
+      // drain: all issued MMAs complete before TMEM is released
+      ptx::mma_commit(mdone);
+      wait_bounded(mdone, 0, abort_flag, p, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+      const Tile ti = decode(p, t);
+      const NsGroup& G = p.g[ti.g];
+      const int acc = it & 1;
+      const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, p, true) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      const int r = ti.tm * BM + row_in_tile;
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        float v[32];
+        ptx::tmem_ld_32x32b_x32(tbase + ch * 32, v);
+        epilogue_chunk(p, G, ti, r, ti.tn * BN + ch * 32, v);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace tc
+
+int ns_tc_smem_bytes() { return tc::SMEM_BYTES; }
+
+cudaError_t launch_ns_tc(const NsParams& p, cudaStream_t s, int num_sms) {
+  if (p.total_tiles <= 0) return cudaSuccess;
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(tc::ns_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
+  tc::ns_tc_kernel<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// host: tensor maps (driver entry point through the runtime, no -lcuda)
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeTiledFn) nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {dim0, dim1, dim2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace muon

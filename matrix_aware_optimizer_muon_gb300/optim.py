@@ -1,0 +1,51 @@
+"""Stateful wrapper: momentum buffers, workspace and step counter around muon_periodic_step."""
+from __future__ import annotations
+
+from typing import Dict, List, Sequence
+
+import torch
+
+from . import _lib
+
+
+class PeriodicMuon:
+    """Periodic Row-wise Muon over a list of 2-D weight tensors (K = 1 is vanilla Muon).
+
+    State is the fp32 momentum of every matrix and the integer step, which decides
+    the branch (Newton-Schulz refresh when step % K == 0, RowNorm otherwise).
+    """
+
+    def __init__(self, params: Sequence[torch.Tensor], K: int = 3, gamma: float = 0.15, mu: float = 0.95,
+                 eta: float = 0.02, lam: float = 0.01, ns5_mode: str = "bf16"):
+        self.params: List[torch.Tensor] = list(params)
+        if not self.params:
+            raise ValueError("no parameters")
+        self.K, self.gamma, self.mu, self.eta, self.lam, self.ns5_mode = K, gamma, mu, eta, lam, ns5_mode
+        dev = self.params[0].device
+        self.M = [torch.zeros(p.shape, dtype=torch.float32, device=dev) for p in self.params]
+        self.ws = _lib.alloc_workspace([tuple(p.shape) for p in self.params], ns5_mode, device=dev)
+        self.step_count = 0
+
+    def step(self, grads: Sequence[torch.Tensor], stream=None) -> int:
+        br = _lib.muon_periodic_step(self.params, grads, self.M, self.step_count, self.ws, K=self.K,
+                                     gamma=self.gamma, mu=self.mu, eta=self.eta, lam=self.lam,
+                                     ns5_mode=self.ns5_mode, stream=stream)
+        self.step_count += 1
+        return br
+
+    def check(self, stream=None) -> int:
+        return _lib.muon_check_status(self.ws, stream)
+
+    def state_dict(self) -> Dict:
+        return {"step": self.step_count, "M": [m.detach().clone() for m in self.M],
+                "hyper": dict(K=self.K, gamma=self.gamma, mu=self.mu, eta=self.eta, lam=self.lam,
+                              ns5_mode=self.ns5_mode)}
+
+    def load_state_dict(self, sd: Dict) -> None:
+        if len(sd["M"]) != len(self.M):
+            raise ValueError("state has a different number of matrices")
+        for dst, src in zip(self.M, sd["M"]):
+            if tuple(dst.shape) != tuple(src.shape):
+                raise ValueError("state shape mismatch")
+            dst.copy_(src)
+        self.step_count = int(sd["step"])

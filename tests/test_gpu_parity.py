@@ -1,0 +1,367 @@
+"""GPU parity: every entry point of the C ABI against the fp64 oracle, element by
+element on the same seeded inputs, at sizes spanning several tiles with ragged
+tails, plus edge cases (empty, 1 x n, n x 1, zero lines, zero matrices)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import muon_ref
+from parity_util import (SCALES8, TOL_F32, TOL_NS5_BF16, TOL_NS5_F32, assert_bf16_within_ulp, assert_f32_close,
+                         dev, inputs, rel_fro, to_dev, to_np)
+from synth import gradient_np, quantize_np
+
+pytestmark = pytest.mark.gpu
+
+mm = pytest.importorskip("matrix_aware_optimizer_muon_gb300")
+
+SHAPES_EW = [(256, 1024), (300, 1000), (1000, 300), (64, 128), (7, 13), (13, 7), (1, 1), (1, 517), (517, 1),
+             (129, 129), (65, 130)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mm.load_library()
+    torch.cuda.set_device(0)
+    yield
+    mm.muon_debug_set(0, 0)
+
+
+def rand_M(shapes, seed=3, zero_line=False):
+    rng = np.random.default_rng(seed)
+    out = []
+    for (a, b) in shapes:
+        M = (rng.standard_normal((a, b)) * 1e-2).astype(np.float32)
+        if zero_line and a > 2 and b > 2:
+            if a <= b:
+                M[1, :] = 0.0
+            else:
+                M[:, 1] = 0.0
+        out.append(M)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# momentum and Frobenius norm
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_momentum_parity(gdt):
+    shapes = SHAPES_EW
+    M0 = rand_M(shapes)
+    _, Gs = inputs(shapes, "bf16", gdt, 1)
+    G = [to_dev(g, gdt) for g in Gs[0]]
+    M = [to_dev(m, "f32") for m in M0]
+    ws = mm.alloc_workspace(shapes)
+    fro = torch.full((len(shapes),), -1.0, device=dev())
+    mm.muon_momentum(G, M, 0.95, fro, ws)
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        ref = muon_ref.momentum(M0[i], Gs[0][i], 0.95)
+        assert_f32_close(to_np(M[i]), ref, what=f"M {shapes[i]}")
+        want = float(np.sum(ref * ref))
+        assert abs(float(fro[i]) - want) <= TOL_F32 * want, (shapes[i], float(fro[i]), want)
+    # without the norm output (no workspace needed)
+    M2 = [to_dev(m, "f32") for m in M0]
+    mm.muon_momentum(G, M2, 0.9)
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        assert_f32_close(to_np(M2[i]), muon_ref.momentum(M0[i], Gs[0][i], 0.9), what="M mu=0.9")
+
+
+def test_fro_norm_parity():
+    shapes = SHAPES_EW + [(3, 40000)]
+    M0 = rand_M(shapes, seed=4)
+    M0[2][:] = 0.0
+    M = [to_dev(m, "f32") for m in M0]
+    ws = mm.alloc_workspace(shapes)
+    out = torch.full((len(shapes),), -1.0, device=dev())
+    mm.muon_fro_norm(M, out, ws)
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        want = muon_ref.frobenius_norm(M0[i])
+        assert abs(float(out[i]) - want) <= TOL_F32 * max(want, 1e-30), shapes[i]
+
+
+# ---------------------------------------------------------------------------
+# RowNorm and apply
+# ---------------------------------------------------------------------------
+def test_rownorm_parity():
+    shapes = SHAPES_EW + [(4, 20000), (20000, 4)]
+    M0 = rand_M(shapes, seed=5, zero_line=True)
+    M = [to_dev(m, "f32") for m in M0]
+    R = [torch.full(s, 7.0, device=dev()) for s in shapes]
+    ws = mm.alloc_workspace(shapes)
+    mm.muon_rownorm(M, R, ws)
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        ref = muon_ref.rownorm(M0[i])
+        assert_f32_close(to_np(R[i]), ref, what=f"R {shapes[i]}")
+        assert np.array_equal(to_np(M[i]), M0[i].astype(np.float64))  # M untouched
+
+
+@pytest.mark.parametrize("wdt,udt", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "f32"), ("f32", "bf16")])
+def test_apply_parity(wdt, udt):
+    shapes = SHAPES_EW
+    W0, _ = inputs(shapes, wdt, "bf16", 0)
+    rng = np.random.default_rng(6)
+    U0 = [quantize_np((rng.standard_normal(s) * 0.05).astype(np.float32), udt) for s in shapes]
+    W = [to_dev(w, wdt) for w in W0]
+    U = [to_dev(u, udt) for u in U0]
+    mm.muon_apply(W, U, 0.2, 0.02, 0.01)
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(shapes):
+        s = 0.2 * math.sqrt(max(a, b))
+        ref = muon_ref.apply_update(W0[i], U0[i], s, 0.02, 0.01)
+        if wdt == "f32":
+            assert_f32_close(to_np(W[i]), ref, what=f"W {shapes[i]}")
+        else:
+            assert_bf16_within_ulp(to_np(W[i]), ref, what=f"W {shapes[i]}")
+
+
+# ---------------------------------------------------------------------------
+# RowNorm step (fused momentum + RowNorm + apply), wide and tall, ragged
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_rownorm_step_parity(dt):
+    shapes = [(256, 1024), (300, 1000), (1000, 300), (1536, 1536), (7, 13), (13, 7), (1, 517), (517, 1),
+              (3, 20000), (129, 129)]
+    W0, Gs = inputs(shapes, dt, dt, 2)
+    M0 = rand_M(shapes, seed=8, zero_line=True)
+    W = [to_dev(w, dt) for w in W0]
+    M = [to_dev(m, "f32") for m in M0]
+    G = [to_dev(g, dt) for g in Gs[1]]
+    ws = mm.alloc_workspace(shapes)
+    br = mm.muon_periodic_step(W, G, M, 1, ws, K=3)
+    assert br == mm.MUON_BRANCH_ROWNORM
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        refW, refM, refresh = muon_ref.periodic_step(W0[i], M0[i], Gs[1][i], 1, 3, 0.15, 0.95, 0.02, 0.01)
+        assert not refresh
+        assert_f32_close(to_np(M[i]), refM, what=f"M {shapes[i]}")
+        if dt == "f32":
+            assert_f32_close(to_np(W[i]), refW, what=f"W {shapes[i]}")
+        else:
+            assert_bf16_within_ulp(to_np(W[i]), refW, what=f"W {shapes[i]}")
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+
+
+# ---------------------------------------------------------------------------
+# Newton-Schulz
+# ---------------------------------------------------------------------------
+NS_SHAPES = [(256, 1024), (1024, 256), (300, 1000), (1000, 300), (520, 1100), (384, 384), (130, 2000),
+             (33, 100), (100, 33), (1, 64), (64, 1), (8, 8)]
+
+
+def mixed_momentum(shape, steps, seed=0):
+    a, b = shape
+    M = np.zeros((a, b))
+    for t in range(steps):
+        M = 0.95 * M + quantize_np(gradient_np(a, b, SCALES8, seed, 0, t), "bf16")
+    return M.astype(np.float32)
+
+
+@pytest.mark.parametrize("mode,tol", [("bf16", TOL_NS5_BF16), ("f32", TOL_NS5_F32)])
+@pytest.mark.parametrize("steps", [1, 4])
+def test_ns5_parity(mode, tol, steps):
+    shapes = NS_SHAPES
+    M0 = [mixed_momentum(s, steps, seed=i) for i, s in enumerate(shapes)]
+    M = [to_dev(m, "f32") for m in M0]
+    odt = torch.bfloat16 if mode == "bf16" else torch.float32
+    O = [torch.full(s, 9.0, device=dev(), dtype=odt) for s in shapes]
+    ws = mm.alloc_workspace(shapes, mode)
+    mm.muon_ns5_batched(M, O, ws, ns5_mode=mode)
+    torch.cuda.synchronize()
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+    worst = 0.0
+    for i in range(len(shapes)):
+        ref = muon_ref.newton_schulz(M0[i].astype(np.float64))
+        err = rel_fro(to_np(O[i]), ref)
+        worst = max(worst, err)
+        assert err <= tol, (shapes[i], err)
+        assert np.array_equal(to_np(M[i]), M0[i].astype(np.float64))
+    print(f"ns5 {mode} steps={steps}: worst relative Frobenius error {worst:.3e}")
+
+
+def test_ns5_zero_matrix_and_scale_invariance():
+    shapes = [(64, 128), (128, 64), (300, 1000)]
+    M0 = [np.zeros(shapes[0], np.float32), mixed_momentum(shapes[1], 1), mixed_momentum(shapes[2], 1)]
+    M1 = [m * np.float32(64.0) for m in M0]   # exact power-of-two scaling
+    O0 = [torch.empty(s, device=dev(), dtype=torch.bfloat16) for s in shapes]
+    O1 = [torch.empty(s, device=dev(), dtype=torch.bfloat16) for s in shapes]
+    ws = mm.alloc_workspace(shapes)
+    mm.muon_ns5_batched([to_dev(m, "f32") for m in M0], O0, ws)
+    mm.muon_ns5_batched([to_dev(m, "f32") for m in M1], O1, ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(O0[0]).item() == 0
+    for i in (1, 2):
+        assert torch.equal(O0[i], O1[i]), "NS5 must be invariant to a power-of-two scale of M"
+
+
+# ---------------------------------------------------------------------------
+# whole refresh step with the apply fused into the last GEMM
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt,mode", [("bf16", "bf16"), ("f32", "f32"), ("bf16", "f32"), ("f32", "bf16")])
+def test_refresh_step_parity(dt, mode):
+    shapes = [(256, 1024), (1024, 256), (300, 1000), (1000, 300), (129, 129), (33, 100)]
+    W0, Gs = inputs(shapes, dt, dt, 1)
+    M0 = [mixed_momentum(s, 3, seed=10 + i) for i, s in enumerate(shapes)]
+    W = [to_dev(w, dt) for w in W0]
+    M = [to_dev(m, "f32") for m in M0]
+    G = [to_dev(g, dt) for g in Gs[0]]
+    ws = mm.alloc_workspace(shapes, mode)
+    br = mm.muon_periodic_step(W, G, M, 3, ws, K=3, ns5_mode=mode)
+    assert br == mm.MUON_BRANCH_NS5
+    torch.cuda.synchronize()
+    tol = TOL_NS5_BF16 if mode == "bf16" else TOL_NS5_F32
+    for i, (a, b) in enumerate(shapes):
+        refW, refM, refresh = muon_ref.periodic_step(W0[i], M0[i], Gs[0][i], 3, 3, 0.15, 0.95, 0.02, 0.01)
+        assert refresh
+        assert_f32_close(to_np(M[i]), refM, what=f"M {shapes[i]}")
+        dW = refW - W0[i]
+        got = to_np(W[i])
+        # update error within the NS5 tolerance, plus the storage rounding of W
+        ulp = 2.0 ** -23 if dt == "f32" else 2.0 ** -7
+        round_budget = np.linalg.norm(np.abs(refW)) * ulp
+        assert np.linalg.norm(got - refW) <= tol * np.linalg.norm(dW) + round_budget, shapes[i]
+
+
+# ---------------------------------------------------------------------------
+# schedule, determinism, resume, vanilla Muon
+# ---------------------------------------------------------------------------
+def run_steps(shapes, dt, steps, K=3, mode="bf16", start_state=None, start_step=0, seed=0):
+    W0, Gs = inputs(shapes, dt, dt, start_step + steps, seed=seed)
+    if start_state is None:
+        W = [to_dev(w, dt) for w in W0]
+        M = [torch.zeros(s, device=dev()) for s in shapes]
+    else:
+        W, M = [w.clone() for w in start_state[0]], [m.clone() for m in start_state[1]]
+    ws = mm.alloc_workspace(shapes, mode)
+    branches = []
+    for t in range(start_step, start_step + steps):
+        G = [to_dev(g, dt) for g in Gs[t]]
+        branches.append(mm.muon_periodic_step(W, G, M, t, ws, K=K, ns5_mode=mode))
+    torch.cuda.synchronize()
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+    return W, M, branches
+
+
+def test_determinism_bit_exact():
+    shapes = [(300, 1000), (1000, 300), (256, 256)]
+    W1, M1, b1 = run_steps(shapes, "bf16", 4)
+    W2, M2, b2 = run_steps(shapes, "bf16", 4)
+    assert b1 == b2 == [1, 0, 0, 1]
+    for a, b in zip(W1 + M1, W2 + M2):
+        assert torch.equal(a, b)
+
+
+def test_resume_bit_exact():
+    shapes = [(300, 1000), (1000, 300)]
+    Wa, Ma, _ = run_steps(shapes, "bf16", 6)
+    Wb, Mb, _ = run_steps(shapes, "bf16", 3)
+    state = ([w.cpu().clone() for w in Wb], [m.cpu().clone() for m in Mb])   # checkpoint to host
+    state = ([w.to(dev()) for w in state[0]], [m.to(dev()) for m in state[1]])
+    Wc, Mc, br = run_steps(shapes, "bf16", 3, start_state=state, start_step=3)
+    assert br == [1, 0, 0]
+    for a, b in zip(Wa + Ma, Wc + Mc):
+        assert torch.equal(a, b)
+
+
+def test_vanilla_K1_every_step_refreshes():
+    shapes = [(64, 256), (256, 64)]
+    _, _, br = run_steps(shapes, "bf16", 4, K=1)
+    assert br == [1, 1, 1, 1]
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+def test_empty_and_degenerate():
+    assert mm.muon_periodic_step([], [], [], 0, torch.empty(256, dtype=torch.uint8, device=dev())) == 1
+    shapes = [(0, 16), (16, 0), (1, 1), (1, 300), (300, 1)]
+    W0, Gs = inputs(shapes, "bf16", "bf16", 2)
+    W = [to_dev(w, "bf16") for w in W0]
+    M = [torch.zeros(s, device=dev()) for s in shapes]
+    ws = mm.alloc_workspace(shapes)
+    refW = [w.astype(np.float64) for w in W0]
+    refM = [np.zeros(s) for s in shapes]
+    for t in range(2):
+        G = [to_dev(g, "bf16") for g in Gs[t]]
+        mm.muon_periodic_step(W, G, M, t, ws)
+        for i in range(len(shapes)):
+            refW[i], refM[i], _ = muon_ref.periodic_step(refW[i], refM[i], Gs[t][i], t, w_dtype="bf16")
+    torch.cuda.synchronize()
+    for i, s in enumerate(shapes):
+        if 0 in s:
+            continue
+        assert_f32_close(to_np(M[i]), refM[i], what=f"M {s}")
+        # a 1 x n or n x 1 matrix: NS5 of a rank-1 input, RowNorm of one line
+        assert np.linalg.norm(to_np(W[i]) - refW[i]) <= 3e-2 * np.linalg.norm(refW[i] - W0[i]) + \
+            np.linalg.norm(np.abs(refW[i])) * 2.0 ** -8, s
+
+
+def test_zero_gradient_is_pure_weight_decay():
+    shapes = [(64, 128), (128, 64)]
+    W0, _ = inputs(shapes, "f32", "f32", 0)
+    W = [to_dev(w, "f32") for w in W0]
+    M = [torch.zeros(s, device=dev()) for s in shapes]
+    G = [torch.zeros(s, device=dev()) for s in shapes]
+    ws = mm.alloc_workspace(shapes, "f32")
+    for t in range(3):
+        mm.muon_periodic_step(W, G, M, t, ws, ns5_mode="f32")
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert_f32_close(to_np(W[i]), W0[i] * (1 - 0.02 * 0.01) ** 3, what="decay")
+
+
+def test_misaligned_views_take_the_scalar_path():
+    """Row length not a multiple of 4 and a base offset by one element.
+
+    Teacher-forced: before each step the GPU state is set to the oracle's state."""
+    shape = (37, 53)
+    n = shape[0] * shape[1]
+    base_w = torch.zeros(1 + n, dtype=torch.bfloat16, device=dev())
+    base_g = torch.zeros(1 + n, dtype=torch.bfloat16, device=dev())
+    base_m = torch.zeros(1 + n, dtype=torch.float32, device=dev())
+    W0, Gs = inputs([shape], "bf16", "bf16", 3)
+    W, G, M = base_w[1:].view(shape), base_g[1:].view(shape), base_m[1:].view(shape)
+    ws = mm.alloc_workspace([shape])
+    refW, refM = W0[0].astype(np.float64), np.zeros(shape)
+    for t in range(3):
+        W.copy_(to_dev(refW.astype(np.float32), "bf16"))
+        M.copy_(to_dev(refM.astype(np.float32), "f32"))
+        G.copy_(to_dev(Gs[t][0], "bf16"))
+        mm.muon_periodic_step([W], [G], [M], t, ws)
+        prevW = refW
+        refW, refM, refresh = muon_ref.periodic_step(refW, refM.astype(np.float32), Gs[t][0], t, w_dtype="bf16")
+        torch.cuda.synchronize()
+        assert_f32_close(to_np(M), refM, what=f"M step {t}")
+        if refresh:
+            assert np.linalg.norm(to_np(W) - refW) <= TOL_NS5_BF16 * np.linalg.norm(refW - prevW) + \
+                np.linalg.norm(np.abs(refW)) * 2.0 ** -8
+        else:
+            assert_bf16_within_ulp(to_np(W), muon_ref.apply_update(
+                prevW, muon_ref.rownorm(refM), muon_ref.update_scale(*shape, False, 0.15), 0.02, 0.01),
+                what=f"W step {t}")
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+
+
+# ---------------------------------------------------------------------------
+# device-side bounded waits: an expired wait is reported, the context survives
+# ---------------------------------------------------------------------------
+def test_stalled_producer_times_out_and_context_survives():
+    shapes = [(256, 512)]
+    M = [to_dev(mixed_momentum(shapes[0], 1), "f32")]
+    O = [torch.empty(shapes[0], device=dev(), dtype=torch.bfloat16)]
+    ws = mm.alloc_workspace(shapes)
+    mm.muon_debug_set(mm.MUON_DEBUG_STALL_PRODUCER, 50)
+    try:
+        mm.muon_ns5_batched(M, O, ws)
+        assert mm.muon_check_status(ws) == mm.MUON_ERR_TIMEOUT
+    finally:
+        mm.muon_debug_set(0, 0)
+    # the status word was cleared and the context still works
+    mm.muon_ns5_batched(M, O, ws)
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+    ref = muon_ref.newton_schulz(to_np(M[0]))
+    assert rel_fro(to_np(O[0]), ref) <= TOL_NS5_BF16
