@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--matrices", type=int, default=0,
+                    help="keep only the first N matrices of the set (small cases for profiling)")
     return ap.parse_args()
 
 
@@ -187,12 +189,20 @@ def oracle_sample(wl, seed=0):
     return total * 1e3, detail
 
 
+def select_workload(args):
+    import dataclasses
+    from synth import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    if args.matrices and args.matrices < len(wl.matrices):
+        wl = dataclasses.replace(wl, key=f"{wl.key}[:{args.matrices}]", matrices=wl.matrices[:args.matrices])
+    return wl
+
+
 def run_reference(args, torch):
     rank, world, dist = dist_init(torch)
     if rank != 0:
         return
-    from synth import WORKLOADS
-    wl = WORKLOADS[args.workload]
+    wl = select_workload(args)
     for _ in range(min(args.warmup, 1)):   # the oracle needs no more warm-up than one pass
         oracle_sample(wl)
     vals = []
@@ -227,7 +237,7 @@ def run_ours(args, torch):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     mm.load_library()
-    wl = WORKLOADS[args.workload]
+    wl = select_workload(args)
     shapes = [(m.rows, m.cols) for m in wl.matrices]
     wdt = torch.bfloat16 if wl.w_dtype == "bf16" else torch.float32
     gdt = torch.bfloat16 if wl.g_dtype == "bf16" else torch.float32

@@ -67,6 +67,23 @@ def assert_bf16_within_ulp(got, ref_exact, ulps=1.0, what=""):
     assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} beyond {ulps} ulp; worst {float(np.max(diff / lim))}"
 
 
+def apply_terms(W_old, U, s, eta, lam):
+    """Magnitudes of the summands of W - eta*(s*U + lambda*W), elementwise."""
+    W_old = np.abs(np.asarray(W_old, dtype=np.float64))
+    return W_old * (1.0 + eta * lam) + eta * s * np.abs(np.asarray(U, dtype=np.float64))
+
+
+def assert_bf16_close(got, ref_exact, terms, what=""):
+    """bf16 result of an fp32 update: within 1 bf16 ulp of the exact result plus the
+    fp32 tolerance (1e-5) on the magnitudes of the summed terms.  The second part
+    matters only where the terms cancel and the result is much smaller than them."""
+    got = np.asarray(got, dtype=np.float64)
+    lim = bf16_ulp(ref_exact) + TOL_F32 * np.asarray(terms, dtype=np.float64) + 1e-30
+    diff = np.abs(got - ref_exact)
+    bad = diff > lim
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} beyond 1 ulp + 1e-5*terms; worst {float(np.max(diff / lim))}"
+
+
 def rel_fro(got, ref):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
