@@ -102,6 +102,24 @@ int muon_momentum(const muon_matrix* mats, int n, float mu, float* fro_sq_out,
 int muon_fro_norm(const muon_matrix* mats, int n, float* fro_out,
                   void* ws, size_t ws_bytes, muon_stream_t stream);
 
+/* Same result as muon_fro_norm, for callers that cannot allocate device memory
+ * (for example a plugin inside a host framework that owns every device
+ * allocation, or code that must not call cudaMalloc mid-step because it would
+ * synchronise the device).  The pages have no counterpart: this is a deployment
+ * variant of the norm above.
+ *  - No workspace: the per-tile partial sums live in a fixed 4 MiB array inside
+ *    the library, resident on every GPU that loads it until the process exits.
+ *  - Limit: at most 2^20 tiles of 64 x 128 elements per call (about 8.6e9
+ *    elements of M in total); larger lists return MUON_ERR_UNSUPPORTED.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls share the array.  Calls that overlap on the GPU (different
+ *    streams, or different host threads) race on it; serialise them.
+ *  - Allocates nothing, reads M only, writes fro_out[i] = ||M_i||_F.  Does not
+ *    update muon_launch_count. */
+int muon_fro_norm_noalloc(const muon_matrix* mats, int n, float* fro_out, muon_stream_t stream);
+
 /* Newton-Schulz-5 of the current momentum, Eq. (2) of the "Muon is Scalable"
  * notes: O_i = NS5(M_i), computed on the short side of M_i and returned in
  * M_i's A x B orientation.  O_out: host array of n device pointers, each an

@@ -7,7 +7,7 @@ from ._lib import (MUON_BRANCH_NS5, MUON_BRANCH_ROWNORM, MUON_DEBUG_STALL_PRODUC
                    MUON_DTYPE_F32, MUON_ERR_CUDA, MUON_ERR_INVALID, MUON_ERR_NO_DEVICE, MUON_ERR_TIMEOUT,
                    MUON_ERR_UNSUPPORTED, MUON_ERR_WORKSPACE, MUON_NS5_BF16, MUON_NS5_F32, MUON_OK, MuonError,
                    MuonMatrix, alloc_workspace, load_library, make_matrices, muon_apply, muon_check_status,
-                   muon_debug_set, muon_fro_norm, muon_momentum, muon_ns5_batched, muon_periodic_step,
+                   muon_debug_set, muon_fro_norm, muon_fro_norm_noalloc, muon_momentum, muon_ns5_batched, muon_periodic_step,
                    muon_rownorm, muon_workspace_init, muon_workspace_size, status_str,
                    muon_profile_events, muon_launch_count)
 from .optim import PeriodicMuon

@@ -64,6 +64,7 @@ def load_library(path: Optional[str] = None):
         "muon_workspace_size": (sz, [mp, i32, i32]),
         "muon_momentum": (i32, [mp, i32, f32, vp, vp, sz, vp]),
         "muon_fro_norm": (i32, [mp, i32, vp, vp, sz, vp]),
+        "muon_fro_norm_noalloc": (i32, [mp, i32, vp, vp]),
         "muon_ns5_batched": (i32, [mp, i32, i32, ptrs, i32, vp, sz, vp]),
         "muon_rownorm": (i32, [mp, i32, ptrs, vp, sz, vp]),
         "muon_apply": (i32, [mp, i32, ptrs, i32, f32, f32, f32, vp]),
@@ -203,6 +204,12 @@ def muon_fro_norm(M: Sequence[torch.Tensor], fro_out: torch.Tensor, ws: torch.Te
     arr, n = make_matrices(M)
     _check("muon_fro_norm", load_library().muon_fro_norm(arr, n, _ptr(fro_out), _ptr(ws), ws.numel(),
                                                          _stream(stream)))
+
+
+def muon_fro_norm_noalloc(M: Sequence[torch.Tensor], fro_out: torch.Tensor, stream=None):
+    """||M_i||_F without a workspace (scratch fixed inside the library)."""
+    arr, n = make_matrices(M)
+    _check("muon_fro_norm_noalloc", load_library().muon_fro_norm_noalloc(arr, n, _ptr(fro_out), _stream(stream)))
 
 
 def muon_ns5_batched(M: Sequence[torch.Tensor], O: Sequence[torch.Tensor], ws: torch.Tensor,
