@@ -436,8 +436,10 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
             prm.dst[mbase + q] = dst_ptrs ? dst_ptrs[li] : nullptr;
             const muon_matrix& a = mats[li];
             prm.msrc[mbase + q] = a.M;
+            const void* dptr = dst_ptrs ? dst_ptrs[li] : nullptr;
             prm.flags[mbase + q] = (unsigned char)((a.rows > a.cols ? NS_TALL : 0) |
-                                                   ((a.cols % 4 == 0 && aligned(a.M, 16)) ? NS_MVEC : 0));
+                                                   ((a.cols % 4 == 0 && aligned(a.M, 16)) ? NS_MVEC : 0) |
+                                                   ((a.rows <= a.cols && a.cols % 8 == 0 && aligned(dptr, 16)) ? NS_WVEC : 0));
           }
           mbase += g.count;
         }

@@ -120,7 +120,7 @@ struct LineFinalParams {
 // Newton-Schulz GEMMs
 // ---------------------------------------------------------------------------
 enum GemmKind : int { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_UPDATE = 2 };
-enum NsFlags : int { NS_TALL = 1, NS_MVEC = 2 };
+enum NsFlags : int { NS_TALL = 1, NS_MVEC = 2, NS_WVEC = 4 };
 // Iterations 1..NS_LO_ITERS add a bf16 residual to the bf16 X in the a*X term
 // (X carried with ~16 significant bits where the small singular directions are
 // still far below the element magnitudes).
@@ -162,7 +162,7 @@ struct NsParams {
   // last-iteration outputs, per matrix (launch table order)
   void* dst[NS_MAX_MATS];  // W (apply) or O (output)
   const float* msrc[NS_MAX_MATS];  // fp32 momentum, the exact X0 for the first a*X term
-  unsigned char flags[NS_MAX_MATS];  // NS_TALL | NS_MVEC
+  unsigned char flags[NS_MAX_MATS];  // NS_TALL | NS_MVEC | NS_WVEC
   int dst_mode;            // 0: O in dst_dtype; 1: apply to W of dst_dtype
   int dst_dtype;           // MUON_DTYPE_*
   float eta, lam, rms_match;

@@ -38,8 +38,9 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
-constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half of the columns
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int EPI_CHUNKS = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per epilogue warp
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr uint32_t DEV_TIMEOUT = 1u;
@@ -118,9 +119,83 @@ __device__ __forceinline__ void load_bf16x32(const bf16* src, float (&v)[32]) {
   }
 }
 
-// Epilogue for 32 consecutive columns [c0, c0+32) of row r of one tile.
-__device__ __forceinline__ void epilogue_chunk(const NsParams& p, const NsGroup& G, const Tile& ti, int r,
-                                               int c0, float (&v)[32]) {
+// Global inputs of one epilogue chunk (32 consecutive columns of one row),
+// loaded one chunk ahead so that the loads overlap the previous chunk's work.
+// Only full, vector-aligned chunks are prefetched; ragged chunks at a matrix
+// edge load element by element in epi_finish.
+struct ChunkIn {
+  uint32_t w[32];
+  bool ok;
+};
+
+__device__ __forceinline__ void ld_u4x4(const void* src, uint32_t* w) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = reinterpret_cast<const uint4*>(src)[q];
+    w[4 * q] = u.x; w[4 * q + 1] = u.y; w[4 * q + 2] = u.z; w[4 * q + 3] = u.w;
+  }
+}
+__device__ __forceinline__ void unpack_bf16x32(const uint32_t* w, float (&v)[32]) {
+#pragma unroll
+  for (int h = 0; h < 16; ++h) {
+    v[2 * h] = __uint_as_float(w[h] << 16);
+    v[2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ void epi_prefetch(const NsParams& p, const NsGroup& G, const Tile& ti, int r, int c0,
+                                             ChunkIn& in) {
+  in.ok = false;
+  const int n = G.n, m = G.m;
+  const int gm = G.mat_base + ti.mat;
+  if (p.kind == GEMM_GRAM) return;
+  if (p.kind == GEMM_POLY) {
+    if (r >= n || c0 + 32 > n || r > c0 + 31) return;
+    ld_u4x4(reinterpret_cast<const bf16*>(G.epi_in) + (size_t)ti.mat * G.stride_nn + (size_t)r * G.ld_n + c0, in.w);
+    in.ok = true;
+    return;
+  }
+  if (r >= n || c0 + 32 > m) return;
+  if (p.first_iter) {
+    const float* Mp = p.msrc[gm];
+    if (p.flags[gm] & NS_TALL) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) in.w[j] = __float_as_uint(Mp[(size_t)(c0 + j) * n + r]);
+    } else if (p.flags[gm] & NS_MVEC) {
+      const float4* src = reinterpret_cast<const float4*>(Mp + (size_t)r * m + c0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 f = src[q];
+        in.w[4 * q] = __float_as_uint(f.x); in.w[4 * q + 1] = __float_as_uint(f.y);
+        in.w[4 * q + 2] = __float_as_uint(f.z); in.w[4 * q + 3] = __float_as_uint(f.w);
+      }
+    } else {
+      return;
+    }
+    in.ok = true;
+    return;
+  }
+  const size_t off = (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m + c0;
+  ld_u4x4(reinterpret_cast<const bf16*>(G.epi_in) + off, in.w);
+  if (G.lo_in) {
+    ld_u4x4(reinterpret_cast<const bf16*>(G.lo_in) + off, in.w + 16);
+  } else if (p.last_iter && p.dst_mode == 1 && p.dst_dtype == MUON_DTYPE_BF16) {
+    if (p.flags[gm] & NS_WVEC) {
+      ld_u4x4(reinterpret_cast<const bf16*>(p.dst[gm]) + (size_t)r * m + c0, in.w + 16);
+    } else if (p.flags[gm] & NS_TALL) {
+      // tall W (m x n): W[c][r]; consecutive lanes read consecutive r
+      const unsigned short* Wt = reinterpret_cast<const unsigned short*>(p.dst[gm]) + r;
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        in.w[16 + h] = (uint32_t)Wt[(size_t)(c0 + 2 * h) * n] | ((uint32_t)Wt[(size_t)(c0 + 2 * h + 1) * n] << 16);
+    }
+  }
+  in.ok = true;
+}
+
+// Combine and store 32 consecutive columns [c0, c0+32) of row r of one tile.
+__device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, const Tile& ti, int r, int c0,
+                                           float (&v)[32], const ChunkIn& in) {
   const int n = G.n, m = G.m;
   const int gm = G.mat_base + ti.mat;
   if (p.kind == GEMM_UPDATE) {
@@ -128,43 +203,31 @@ __device__ __forceinline__ void epilogue_chunk(const NsParams& p, const NsGroup&
     const float sc = p.first_iter ? p.inv_norm[gm] : 1.0f;
     const bool full = c0 + 32 <= m;
     float x[32];
-    if (p.first_iter) {
-      // a*X0 from the fp32 momentum itself (X0 = M on the short side)
-      const float* Mp = p.msrc[gm];
-      if (p.flags[gm] & NS_TALL) {
+    if (in.ok && p.first_iter) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = (c0 + j < m) ? Mp[(size_t)(c0 + j) * n + r] : 0.f;
-      } else if (full && (p.flags[gm] & NS_MVEC)) {
-        const float4* src = reinterpret_cast<const float4*>(Mp + (size_t)r * m + c0);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 f = src[q];
-          x[4 * q] = f.x; x[4 * q + 1] = f.y; x[4 * q + 2] = f.z; x[4 * q + 3] = f.w;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = (c0 + j < m) ? Mp[(size_t)r * m + c0 + j] : 0.f;
-      }
-    } else {
-      const bf16* Xin = reinterpret_cast<const bf16*>(G.epi_in) + (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m;
-      if (full) {
-        load_bf16x32(Xin + c0, x);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = (c0 + j < m) ? __bfloat162float(Xin[c0 + j]) : 0.f;
-      }
+      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(in.w[j]);
+    } else if (in.ok) {
+      unpack_bf16x32(in.w, x);
       if (G.lo_in) {
-        const bf16* Lin = reinterpret_cast<const bf16*>(G.lo_in) + (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m;
         float l[32];
-        if (full) {
-          load_bf16x32(Lin + c0, l);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) l[j] = (c0 + j < m) ? __bfloat162float(Lin[c0 + j]) : 0.f;
-        }
+        unpack_bf16x32(in.w + 16, l);
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] += l[j];
       }
+    } else if (p.first_iter) {
+      // a*X0 from the fp32 momentum itself (X0 = M on the short side), ragged edge
+      const float* Mp = p.msrc[gm];
+      const bool tall = p.flags[gm] & NS_TALL;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        x[j] = (c0 + j < m) ? (tall ? Mp[(size_t)(c0 + j) * n + r] : Mp[(size_t)r * m + c0 + j]) : 0.f;
+    } else {
+      const size_t off = (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m;
+      const bf16* Xin = reinterpret_cast<const bf16*>(G.epi_in) + off;
+      const bf16* Lin = G.lo_in ? reinterpret_cast<const bf16*>(G.lo_in) + off : nullptr;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        x[j] = (c0 + j < m) ? __bfloat162float(Xin[c0 + j]) + (Lin ? __bfloat162float(Lin[c0 + j]) : 0.f) : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = sc * (p.a * x[j] + v[j]);
@@ -188,9 +251,26 @@ __device__ __forceinline__ void epilogue_chunk(const NsParams& p, const NsGroup&
       }
     } else {
       const float s_apply = p.rms_match * sqrtf((float)m);
+      if (in.ok && p.dst_mode == 1 && p.dst_dtype == MUON_DTYPE_BF16 && (p.flags[gm] & NS_WVEC)) {
+        // wide bf16 W: W[r][c0..c0+31] as four 16-byte vectors
+        float w[32];
+        unpack_bf16x32(in.w + 16, w);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < m) ns_last_store(p, gm, n, m, r, c0 + j, v[j], s_apply);
+        for (int j = 0; j < 32; ++j) w[j] = w[j] - p.eta * (s_apply * v[j] + p.lam * w[j]);
+        store_bf16x32(reinterpret_cast<bf16*>(p.dst[gm]) + (size_t)r * m + c0, w);
+      } else if (in.ok && p.dst_mode == 1 && p.dst_dtype == MUON_DTYPE_BF16 && (p.flags[gm] & NS_TALL)) {
+        // tall bf16 W: element (r, c) of the short-side result is W[c][r]
+        float w[32];
+        unpack_bf16x32(in.w + 16, w);
+        bf16* Wt = reinterpret_cast<bf16*>(p.dst[gm]) + r;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          Wt[(size_t)(c0 + j) * n] = __float2bfloat16_rn(w[j] - p.eta * (s_apply * v[j] + p.lam * w[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < m) ns_last_store(p, gm, n, m, r, c0 + j, v[j], s_apply);
+      }
     }
     return;
   }
@@ -203,11 +283,11 @@ __device__ __forceinline__ void epilogue_chunk(const NsParams& p, const NsGroup&
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] *= sc;
   } else {
-    const bf16* S = reinterpret_cast<const bf16*>(G.epi_in) + (size_t)ti.mat * G.stride_nn + (size_t)r * G.ld_n;
     float s[32];
-    if (c0 + 32 <= n) {
-      load_bf16x32(S + c0, s);
+    if (in.ok) {
+      unpack_bf16x32(in.w, s);
     } else {
+      const bf16* S = reinterpret_cast<const bf16*>(G.epi_in) + (size_t)ti.mat * G.stride_nn + (size_t)r * G.ld_n;
 #pragma unroll
       for (int j = 0; j < 32; ++j) s[j] = (c0 + j < n) ? __bfloat162float(S[c0 + j]) : 0.f;
     }
@@ -355,7 +435,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int quarter = warp & 3;            // TMEM lanes this warp may access
+    const int half = (warp - 2) >> 2;        // which half of the 256 columns it drains
     const int row_in_tile = quarter * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
@@ -363,17 +444,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
       const NsGroup& G = p.g[ti.g];
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      const int r = ti.tm * BM + row_in_tile;
+      const int cbase = ti.tn * BN + half * (EPI_CHUNKS * 32);
+      ChunkIn in[2];
+      epi_prefetch(p, G, ti, r, cbase, in[0]);   // does not depend on this tile's accumulator
       int ok = 1;
       if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, p, true) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      const int r = ti.tm * BM + row_in_tile;
-      for (int ch = 0; ch < BN / 32; ++ch) {
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * EPI_CHUNKS * 32);
+#pragma unroll
+      for (int k = 0; k < EPI_CHUNKS; ++k) {
         float v[32];
-        ptx::tmem_ld_32x32b_x32(tbase + ch * 32, v);
-        epilogue_chunk(p, G, ti, r, ti.tn * BN + ch * 32, v);
+        ptx::tmem_ld_32x32b_x32(tbase + k * 32, v);
+        if (k + 1 < EPI_CHUNKS) epi_prefetch(p, G, ti, r, cbase + (k + 1) * 32, in[(k + 1) & 1]);
+        epi_finish(p, G, ti, r, cbase + k * 32, v, in[k & 1]);
       }
       ptx::tc_fence_before();
       __syncwarp();
