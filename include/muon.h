@@ -190,8 +190,10 @@ int muon_abi_version(void);
  * timeout_ms: limit of every device-side wait (default 4000 ms; 0 restores it).
  * flags: MUON_DEBUG_STALL_PRODUCER makes the tensor-core GEMM's load warp issue
  * nothing, so that its consumers' bounded waits expire and report
- * MUON_ERR_TIMEOUT through muon_check_status (no fault, no hang). */
-enum { MUON_DEBUG_STALL_PRODUCER = 1 };
+ * MUON_ERR_TIMEOUT through muon_check_status (no fault, no hang).
+ * MUON_DEBUG_NO_CLUSTER sends tall matrices of RowNorm steps through the
+ * two-pass kernels instead of the single-pass cluster kernel (to test both). */
+enum { MUON_DEBUG_STALL_PRODUCER = 1, MUON_DEBUG_NO_CLUSTER = 2 };
 int muon_debug_set(int flags, int timeout_ms);
 
 #ifdef __cplusplus

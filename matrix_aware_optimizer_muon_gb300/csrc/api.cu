@@ -757,6 +757,56 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
       if ((rc = cuda_status(launch_rows(ck.w_dt, ck.g_dt, kv.first, rp, s))) != MUON_OK) return rc;
     }
   }
+  // tall matrices: single pass, one thread-block cluster per column strip
+  if (!(g_debug_flags.load() & MUON_DEBUG_NO_CLUSTER)) {
+    std::map<int, std::vector<int>> tall_by_rows;
+    std::vector<int> rest;
+    for (int i : two_pass) {
+      const muon_matrix& a = mats[i];
+      const bool ok = a.rows > a.cols && a.cols % 4 == 0 && aligned(a.M, 16) && aligned(a.G, 4 * dsize(ck.g_dt)) &&
+                      aligned(a.W, 4 * dsize(ck.w_dt)) && cols_strip_width((int)a.rows) > 0;
+      if (ok) tall_by_rows[(int)a.rows].push_back(i);
+      else rest.push_back(i);
+    }
+    static thread_local ColsParams cp;
+    for (const auto& kv : tall_by_rows) {
+      const std::vector<int>& v = kv.second;
+      const int cw = cols_strip_width(kv.first);
+      size_t k = 0;
+      while (k < v.size()) {
+        const size_t k0 = k;
+        std::memset(&cp, 0, sizeof(cp));
+        cp.mu = mu;
+        cp.eta = eta;
+        cp.lam = lambda;
+        cp.slab_max = (kv.first + cols_cluster_size() - 1) / cols_cluster_size();
+        int j = 0, units = 0;
+        for (; k < v.size() && j < COLS_MAX_MATS; ++k) {
+          const muon_matrix& a = mats[v[k]];
+          ColsMat& e = cp.mat[j++];
+          e.W = a.W;
+          e.G = a.G;
+          e.M = a.M;
+          e.rows = (int)a.rows;
+          e.cols = (int)a.cols;
+          e.unit_begin = units;
+          e.scale = gamma * kRmsMatch * std::sqrt((float)a.rows);
+          units += cdiv(a.cols, cw);
+        }
+        cp.nmat = j;
+        cp.total_units = units;
+        const cudaError_t e = launch_cols(ck.w_dt, ck.g_dt, cw, cp, s);
+        if (e == cudaErrorInvalidClusterSize) {
+          // the cluster shape does not fit this device: these go the two-pass way
+          cudaGetLastError();
+          rest.insert(rest.end(), v.begin() + (long)k0, v.begin() + (long)k);
+          continue;
+        }
+        if ((rc = cuda_status(e)) != MUON_OK) return rc;
+      }
+    }
+    two_pass.swap(rest);
+  }
   if (!two_pass.empty()) {
     auto fill = [&](EwMat& e, int i) {
       const MatPlan& mp = P.mats[i];

@@ -248,7 +248,7 @@ __device__ __forceinline__ int find_mat_rows(const RowsParams& p, int t) {
 }
 
 template <typename WT, typename GT, int CPT>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(1024)
 rows_kernel(const __grid_constant__ RowsParams p) {
   __shared__ float red[32];
   const int rg = blockIdx.x;
@@ -427,15 +427,17 @@ cudaError_t launch_ew(int mode, int w_dt, int g_dt, int x_dt, const EwParams& p,
 
 template <typename WT, typename GT>
 static cudaError_t launch_rows_t(int max_cols, const RowsParams& p, cudaStream_t s) {
+  // At most 3-4 four-element chunks per thread keeps registers low and many
+  // threads resident; rows up to 16384 columns use at most 1024 threads.
   const int chunks = (max_cols + 3) / 4;
-  const int T = chunks <= 128 * 8 ? 128 : (chunks <= 256 * 8 ? 256 : 512);
+  int T = ((chunks + 2) / 3 + 31) / 32 * 32;
+  T = T < 64 ? 64 : (T > 1024 ? 1024 : T);
   const int cpt = (chunks + T - 1) / T;
   const dim3 grid(p.total_rows), block(T);
   switch (cpt) {
 #define MUON_ROWS_CASE(C) \
   case (C): rows_kernel<WT, GT, (C)><<<grid, block, 0, s>>>(p); break;
     MUON_ROWS_CASE(1) MUON_ROWS_CASE(2) MUON_ROWS_CASE(3) MUON_ROWS_CASE(4)
-    MUON_ROWS_CASE(5) MUON_ROWS_CASE(6) MUON_ROWS_CASE(7) MUON_ROWS_CASE(8)
 #undef MUON_ROWS_CASE
     default: return cudaErrorInvalidValue;
   }

@@ -74,6 +74,27 @@ struct RowsParams {
   float mu, eta, lam;
 };
 
+// single-pass RowNorm step for tall matrices: one thread-block cluster per
+// column strip, the strip's new momentum held in shared memory
+constexpr int COLS_MAX_MATS = 128;
+constexpr int COLS_MAX_SMEM = 200 * 1024;     // opt-in dynamic shared memory per CTA
+constexpr int COLS_SMEM_TARGET = 112 * 1024;  // two 512-thread CTAs per SM
+struct ColsMat {
+  void* W;
+  const void* G;
+  float* M;
+  int rows, cols;
+  int unit_begin;          // first column strip of this matrix in the launch
+  float scale;
+};
+struct ColsParams {
+  ColsMat mat[COLS_MAX_MATS];
+  int nmat;
+  int total_units;
+  int slab_max;            // rows per CTA slab (ceil(max rows / cluster size))
+  float mu, eta, lam;
+};
+
 // apply from a given direction U
 constexpr int APPLY_MAX_MATS = 128;
 constexpr int APPLY_CHUNK = 4096;  // elements per CTA
@@ -214,6 +235,9 @@ struct Plan {
 cudaError_t launch_ew(int mode, int w_dt, int g_dt, int x_dt, const EwParams& p, cudaStream_t s);
 cudaError_t launch_rows(int w_dt, int g_dt, int max_cols, const RowsParams& p, cudaStream_t s);
 cudaError_t launch_apply(int w_dt, int u_dt, const ApplyParams& p, cudaStream_t s);
+cudaError_t launch_cols(int w_dt, int g_dt, int cw, const ColsParams& p, cudaStream_t s);
+int cols_cluster_size();
+int cols_strip_width(int max_rows);
 cudaError_t launch_fro_final(const FroFinalParams& p, cudaStream_t s);
 cudaError_t launch_line_final(const LineFinalParams& p, cudaStream_t s);
 cudaError_t launch_ns_simt(const NsParams& p, cudaStream_t s);
@@ -234,4 +258,5 @@ static_assert(sizeof(ApplyParams) < 32000, "ApplyParams too large");
 static_assert(sizeof(FroFinalParams) < 32000, "FroFinalParams too large");
 static_assert(sizeof(LineFinalParams) < 32000, "LineFinalParams too large");
 static_assert(sizeof(NsParams) < 32000, "NsParams too large");
+static_assert(sizeof(ColsParams) < 32000, "ColsParams too large");
 }  // namespace muon

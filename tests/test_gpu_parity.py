@@ -122,17 +122,25 @@ def test_apply_parity(wdt, udt):
 # ---------------------------------------------------------------------------
 # RowNorm step (fused momentum + RowNorm + apply), wide and tall, ragged
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("path", ["cluster", "two_pass"])
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
-def test_rownorm_step_parity(dt):
+def test_rownorm_step_parity(dt, path):
+    """Wide rows (single pass), tall columns (cluster single pass, or the two-pass
+    form), ragged and degenerate shapes; (40000, 8) takes 16-column strips and
+    (70000, 8) is too tall for the cluster's shared memory."""
     shapes = [(256, 1024), (300, 1000), (1000, 300), (1536, 1536), (7, 13), (13, 7), (1, 517), (517, 1),
-              (3, 20000), (129, 129)]
+              (3, 20000), (129, 129), (4608, 1536), (300, 36), (40000, 8), (70000, 8), (33, 4)]
     W0, Gs = inputs(shapes, dt, dt, 2)
     M0 = rand_M(shapes, seed=8, zero_line=True)
     W = [to_dev(w, dt) for w in W0]
     M = [to_dev(m, "f32") for m in M0]
     G = [to_dev(g, dt) for g in Gs[1]]
     ws = mm.alloc_workspace(shapes)
-    br = mm.muon_periodic_step(W, G, M, 1, ws, K=3)
+    mm.muon_debug_set(mm.MUON_DEBUG_NO_CLUSTER if path == "two_pass" else 0, 0)
+    try:
+        br = mm.muon_periodic_step(W, G, M, 1, ws, K=3)
+    finally:
+        mm.muon_debug_set(0, 0)
     assert br == mm.MUON_BRANCH_ROWNORM
     torch.cuda.synchronize()
     for i in range(len(shapes)):
