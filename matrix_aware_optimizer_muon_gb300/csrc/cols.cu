@@ -4,8 +4,9 @@
 //
 // A thread-block cluster of CL CTAs owns one strip of CW columns of one matrix;
 // CTA k of the cluster owns rows [k*slab, (k+1)*slab).  Each CTA streams its slab
-// once: M <- mu*M + G is stored to global memory and kept in shared memory,
-// and per-column sums of squares are reduced inside the CTA.  After a cluster
+// once: M <- mu*M + G is kept in shared memory (and written back to global memory
+// in the second phase), and per-column sums of squares are reduced inside the
+// CTA.  After a cluster
 // barrier every CTA adds the CL column partials from its peers' shared memory
 // in rank order (the same order everywhere, so the result is deterministic), and
 // then applies W <- W - eta*(s*M/||column|| + lambda*W) from shared memory.
@@ -21,15 +22,43 @@ namespace muon {
 
 namespace {
 
+// Four consecutive elements as loaded from memory (packed), and their fp32 values.
+template <typename T> struct Raw4;
+template <> struct Raw4<float> { using type = float4; };
+template <> struct Raw4<bf16> { using type = uint2; };
+__device__ __forceinline__ float4 ldraw(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ uint2 ldraw(const bf16* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ float4 ldraw_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ uint2 ldraw_stream(const bf16* p) { return __ldcs(reinterpret_cast<const uint2*>(p)); }
+__device__ __forceinline__ void cvt4(const float4& r, float v[4]) { v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w; }
+__device__ __forceinline__ void cvt4(const uint2& r, float v[4]) {
+  v[0] = __uint_as_float(r.x << 16);
+  v[1] = __uint_as_float(r.x & 0xFFFF0000u);
+  v[2] = __uint_as_float(r.y << 16);
+  v[3] = __uint_as_float(r.y & 0xFFFF0000u);
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_sync_all() {
+// Cluster barrier whose arrival releases this thread's prior writes (used after
+// the column partials are written to shared memory; no global stores are
+// outstanding then, so the release is cheap).
+__device__ __forceinline__ void cluster_sync_release() {
   asm volatile(
       "barrier.cluster.arrive.release.aligned;\n"
       "barrier.cluster.wait.acquire.aligned;\n" ::
+          : "memory");
+}
+// Cluster barrier that orders nothing: it only keeps every CTA's shared memory
+// alive until its peers have finished reading it (those reads completed before
+// the peers arrived, since their values were already used).
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile(
+      "barrier.cluster.arrive.relaxed.aligned;\n"
+      "barrier.cluster.wait.aligned;\n" ::
           : "memory");
 }
 // Load a float from the same shared-memory offset in CTA `rank` of this cluster.
@@ -46,7 +75,8 @@ template <typename WT, typename GT, int CW, int CL, int NT>
 __global__ void __launch_bounds__(NT, 2) cols_cluster_kernel(const __grid_constant__ ColsParams p) {
   constexpr int TPR = CW / 4;       // threads per row (4 columns each)
   constexpr int RPI = NT / TPR;     // rows per pass of the CTA
-  constexpr int UNROLL = 4;
+  constexpr int UNROLL1 = sizeof(GT) == 2 ? 6 : 4;   // rows of M and G in flight per thread
+  constexpr int UNROLL2 = sizeof(WT) == 2 ? 12 : 6;  // rows of W in flight per thread
   extern __shared__ __align__(16) float sm[];
   float* slabM = sm;                                  // [slab][CW]
   float* red = sm + (size_t)p.slab_max * CW;          // [NT/32][CW]
@@ -73,30 +103,34 @@ __global__ void __launch_bounds__(NT, 2) cols_cluster_kernel(const __grid_consta
   const GT* __restrict__ Gg = reinterpret_cast<const GT*>(mt.G);
   WT* __restrict__ Wg = reinterpret_cast<WT*>(mt.W);
 
-  // ---- pass over the slab: momentum, store, column sums of squares
+  // ---- pass over the slab: momentum, store, column sums of squares.
+  // Raw (packed) loads of UNROLL1 rows are issued before any use.
   float cs[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int rb = r0 + trow; rb < r1; rb += RPI * UNROLL) {
-    float v[UNROLL][4];
+  for (int rb = r0 + trow; rb < r1; rb += RPI * UNROLL1) {
+    float4 mr[UNROLL1];
+    typename Raw4<GT>::type gr[UNROLL1];
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
+    for (int u = 0; u < UNROLL1; ++u) {
       const int r = rb + u * RPI;
       if (r < r1 && colok) {
         const size_t off = (size_t)r * B + c0 + tcol;
-        float g[4];
-        ld4(Mg + off, v[u]);
-        ld4_stream(Gg + off, g);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[u][j] = p.mu * v[u][j] + g[j];
+        mr[u] = *reinterpret_cast<const float4*>(Mg + off);
+        gr[u] = ldraw_stream(Gg + off);
       }
     }
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
+    for (int u = 0; u < UNROLL1; ++u) {
       const int r = rb + u * RPI;
       if (r < r1 && colok) {
-        st4(Mg + (size_t)r * B + c0 + tcol, v[u]);
-        st4(slabM + (size_t)(r - r0) * CW + tcol, v[u]);
+        float g[4], v[4];
+        cvt4(gr[u], g);
+        v[0] = p.mu * mr[u].x + g[0];
+        v[1] = p.mu * mr[u].y + g[1];
+        v[2] = p.mu * mr[u].z + g[2];
+        v[3] = p.mu * mr[u].w + g[3];
+        st4(slabM + (size_t)(r - r0) * CW + tcol, v);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) cs[j] = fmaf(v[u][j], v[u][j], cs[j]);
+        for (int j = 0; j < 4; ++j) cs[j] = fmaf(v[j], v[j], cs[j]);
       }
     }
   }
@@ -118,7 +152,7 @@ __global__ void __launch_bounds__(NT, 2) cols_cluster_kernel(const __grid_consta
     colpart[threadIdx.x] = t;
   }
   // ---- cluster: add the CL slab partials in rank order
-  cluster_sync_all();
+  cluster_sync_release();
   if (threadIdx.x < CW) {
     float t = 0.f;
 #pragma unroll
@@ -131,27 +165,29 @@ __global__ void __launch_bounds__(NT, 2) cols_cluster_kernel(const __grid_consta
   float iv[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) iv[j] = inv[tcol + j];
-  for (int rb = r0 + trow; rb < r1; rb += RPI * UNROLL) {
-    float w[UNROLL][4];
+  for (int rb = r0 + trow; rb < r1; rb += RPI * UNROLL2) {
+    typename Raw4<WT>::type wr[UNROLL2];
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
+    for (int u = 0; u < UNROLL2; ++u) {
       const int r = rb + u * RPI;
-      if (r < r1 && colok) ld4(Wg + (size_t)r * B + c0 + tcol, w[u]);
+      if (r < r1 && colok) wr[u] = ldraw(Wg + (size_t)r * B + c0 + tcol);
     }
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
+    for (int u = 0; u < UNROLL2; ++u) {
       const int r = rb + u * RPI;
       if (r < r1 && colok) {
-        float m[4], o[4];
+        float w[4], m[4], o[4];
+        cvt4(wr[u], w);
         ld4(slabM + (size_t)(r - r0) * CW + tcol, m);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[j] = w[u][j] - p.eta * (mt.scale * (m[j] * iv[j]) + p.lam * w[u][j]);
+        for (int j = 0; j < 4; ++j) o[j] = w[j] - p.eta * (mt.scale * (m[j] * iv[j]) + p.lam * w[j]);
+        st4(Mg + (size_t)r * B + c0 + tcol, m);
         st4(Wg + (size_t)r * B + c0 + tcol, o);
       }
     }
   }
   // peers may still be reading this CTA's colpart
-  cluster_sync_all();
+  cluster_sync_relaxed();
 }
 
 constexpr int kCL = 16;
