@@ -36,7 +36,12 @@ def _stale(out, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False) -> str:
+def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False, defines=(), out=None,
+          build_dir=None) -> str:
+    """defines: extra -D flags (tuning variants); out/build_dir: alternative library and object paths."""
+    global BUILD, LIB
+    BUILD = build_dir or os.path.join(HERE, "_build")
+    LIB = out or os.path.join(HERE, "libmuon_gb300.so")
     os.makedirs(BUILD, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(os.path.dirname(HERE), "include", "muon.h"))
@@ -45,7 +50,7 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
         s = os.path.join(CSRC, src)
         o = os.path.join(BUILD, src.replace(".cu", ".o"))
         if force or _stale(o, [s, *headers]):
-            extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+            extra = (["-Xptxas", "-v"] if ptxas_verbose else []) + [f"-D{d}" for d in defines]
             jobs.append((src, [nvcc(), *_flags(extra), "-c", s, "-o", o]))
 
     def run(job):

@@ -361,6 +361,9 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
         prm.c = kNsC;
         prm.first_iter = iter == 0;
         prm.last_iter = (iter == kNsSteps - 1) && kind == GEMM_UPDATE;
+        // Late iterations (X already near its fixed band) take a*X inside the
+        // tensor-core product; the first NS_LO_ITERS + 1 keep a*X in fp32.
+        prm.fold_a = tcmode && iter > NS_LO_ITERS && kind != GEMM_GRAM;
         prm.inv_norm = inv_norm_all + gbase[ch.first];
         prm.dst_mode = dst_mode;
         prm.dst_dtype = dst_dtype;
@@ -761,17 +764,18 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
   if (!(g_debug_flags.load() & MUON_DEBUG_NO_CLUSTER)) {
     std::map<int, std::vector<int>> tall_by_rows;
     std::vector<int> rest;
+    const int stage = (int)std::max(dsize(ck.w_dt), dsize(ck.g_dt));
     for (int i : two_pass) {
       const muon_matrix& a = mats[i];
       const bool ok = a.rows > a.cols && a.cols % 4 == 0 && aligned(a.M, 16) && aligned(a.G, 4 * dsize(ck.g_dt)) &&
-                      aligned(a.W, 4 * dsize(ck.w_dt)) && cols_strip_width((int)a.rows) > 0;
+                      aligned(a.W, 4 * dsize(ck.w_dt)) && cols_strip_width((int)a.rows, stage) > 0;
       if (ok) tall_by_rows[(int)a.rows].push_back(i);
       else rest.push_back(i);
     }
     static thread_local ColsParams cp;
     for (const auto& kv : tall_by_rows) {
       const std::vector<int>& v = kv.second;
-      const int cw = cols_strip_width(kv.first);
+      const int cw = cols_strip_width(kv.first, stage);
       size_t k = 0;
       while (k < v.size()) {
         const size_t k0 = k;

@@ -247,8 +247,9 @@ cudaError_t launch_cols_cw(int w_dt, int g_dt, const ColsParams& p, cudaStream_t
 
 int cols_cluster_size() { return kCL; }
 
-// Widest strip (32 or 16 columns) whose slab fits the shared-memory budget; 0 if none.
-int cols_strip_width(int max_rows) {
+// Widest strip (32 or 16 columns) whose slab of fp32 momentum fits the
+// shared-memory budget; 0 if none.  (The slab holds no G or W.)
+int cols_strip_width(int max_rows, int /*stage_elem_bytes*/) {
   const int slab = (max_rows + kCL - 1) / kCL;
   if (cols_smem_bytes<32>(slab) <= COLS_SMEM_TARGET) return 32;
   if (cols_smem_bytes<16>(slab) <= COLS_MAX_SMEM) return 16;

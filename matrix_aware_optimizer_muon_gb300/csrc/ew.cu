@@ -16,6 +16,11 @@
 #include "common.cuh"
 #include "internal.h"
 
+// Target four-element chunks per thread of the one-row-per-CTA RowNorm kernel.
+#ifndef MUON_ROWS_CPT
+#define MUON_ROWS_CPT 3
+#endif
+
 namespace muon {
 
 template <typename T, int N>
@@ -430,7 +435,7 @@ static cudaError_t launch_rows_t(int max_cols, const RowsParams& p, cudaStream_t
   // At most 3-4 four-element chunks per thread keeps registers low and many
   // threads resident; rows up to 16384 columns use at most 1024 threads.
   const int chunks = (max_cols + 3) / 4;
-  int T = ((chunks + 2) / 3 + 31) / 32 * 32;
+  int T = ((chunks + MUON_ROWS_CPT - 1) / MUON_ROWS_CPT + 31) / 32 * 32;
   T = T < 64 ? 64 : (T > 1024 ? 1024 : T);
   const int cpt = (chunks + T - 1) / T;
   const dim3 grid(p.total_rows), block(T);

@@ -179,6 +179,8 @@ struct NsParams {
   float a, b, c;
   int first_iter;          // fold 1/||M|| (UPDATE) or 1/||M||^2 (GRAM)
   int last_iter;           // UPDATE: write O or apply to W instead of X_out
+  int fold_a;              // POLY writes B + a*I and UPDATE computes (B + a*I) X on the
+                           // tensor cores, without reading X in the epilogue
   const float* inv_norm;   // per matrix (launch table order)
   // last-iteration outputs, per matrix (launch table order)
   void* dst[NS_MAX_MATS];  // W (apply) or O (output)
@@ -237,7 +239,7 @@ cudaError_t launch_rows(int w_dt, int g_dt, int max_cols, const RowsParams& p, c
 cudaError_t launch_apply(int w_dt, int u_dt, const ApplyParams& p, cudaStream_t s);
 cudaError_t launch_cols(int w_dt, int g_dt, int cw, const ColsParams& p, cudaStream_t s);
 int cols_cluster_size();
-int cols_strip_width(int max_rows);
+int cols_strip_width(int max_rows, int stage_elem_bytes);
 cudaError_t launch_fro_final(const FroFinalParams& p, cudaStream_t s);
 cudaError_t launch_line_final(const LineFinalParams& p, cudaStream_t s);
 cudaError_t launch_ns_simt(const NsParams& p, cudaStream_t s);

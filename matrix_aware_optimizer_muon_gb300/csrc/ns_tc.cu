@@ -176,7 +176,7 @@ __device__ __forceinline__ void epi_prefetch(const NsParams& p, const NsGroup& G
     return;
   }
   const size_t off = (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m + c0;
-  ld_u4x4(reinterpret_cast<const bf16*>(G.epi_in) + off, in.w);
+  if (!p.fold_a) ld_u4x4(reinterpret_cast<const bf16*>(G.epi_in) + off, in.w);
   if (G.lo_in) {
     ld_u4x4(reinterpret_cast<const bf16*>(G.lo_in) + off, in.w + 16);
   } else if (p.last_iter && p.dst_mode == 1 && p.dst_dtype == MUON_DTYPE_BF16) {
@@ -203,7 +203,10 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
     const float sc = p.first_iter ? p.inv_norm[gm] : 1.0f;
     const bool full = c0 + 32 <= m;
     float x[32];
-    if (in.ok && p.first_iter) {
+    if (p.fold_a) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = 0.f;   // a*X is already in the accumulator
+    } else if (in.ok && p.first_iter) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(in.w[j]);
     } else if (in.ok) {
@@ -293,6 +296,10 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = p.b * s[j] + p.c * v[j];
+    if (p.fold_a) {   // B + a*I
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] += (c0 + j == r) ? p.a : 0.f;
+    }
   }
   bf16* out = reinterpret_cast<bf16*>(G.out) + (size_t)ti.mat * G.stride_nn;
   if (r <= c0 && c0 + 32 <= n) {

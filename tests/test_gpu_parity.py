@@ -183,14 +183,19 @@ def test_ns5_parity(mode, tol, steps):
     mm.muon_ns5_batched(M, O, ws, ns5_mode=mode)
     torch.cuda.synchronize()
     assert mm.muon_check_status(ws) == mm.MUON_OK
-    worst = 0.0
+    worst = {}
     for i in range(len(shapes)):
         ref = muon_ref.newton_schulz(M0[i].astype(np.float64))
         err = rel_fro(to_np(O[i]), ref)
-        worst = max(worst, err)
+        worst[shapes[i]] = err
         assert err <= tol, (shapes[i], err)
+        # the bf16 path keeps a*X in higher precision in the early iterations; on
+        # matrices spanning several tiles that holds its error near 4e-3
+        # (degenerate 1 x n, n x 1 and 8 x 8 inputs sit near 1.4e-2)
+        if mode == "bf16" and min(shapes[i]) >= 128:
+            assert err <= 1e-2, (shapes[i], err)
         assert np.array_equal(to_np(M[i]), M0[i].astype(np.float64))
-    print(f"ns5 {mode} steps={steps}: worst relative Frobenius error {worst:.3e}")
+    print(f"ns5 {mode} steps={steps}: " + ", ".join(f"{k[0]}x{k[1]} {v:.2e}" for k, v in worst.items()))
 
 
 def test_ns5_zero_matrix_and_scale_invariance():
