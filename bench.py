@@ -29,6 +29,23 @@ METRIC = "Muon optimizer step ms; NS5 TFLOP/s and RowNorm GB/s vs GB300 roofline
 DEFAULT_WORKLOAD = "mmdit-1.3b"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129e6
+# DRAM bytes per ns_tc_kernel launch (read + write, averaged over the 15 launches of
+# a refresh), from ncu dram__bytes_{read,write}.sum on the 20-matrix slice of the
+# set (the same shape mix, 1/8 of the matrices) scaled by 8; see
+# profiles/ns_tc_kernel_traffic_mmdit-1.3b.md.  Valid only for the kernel sources
+# it was measured on (hash below); otherwise the roofline reports null.
+NS5_TRAFFIC = {"mmdit-1.3b": {"bytes_per_launch": 4.70e9, "sources": "49c598b5198ab7fe"}}
+NS5_SOURCES = ["ns_tc.cu", "ns_common.cuh", "ptx.cuh", "common.cuh", "internal.h", "api.cu"]
+
+
+def ns5_sources_hash():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "matrix_aware_optimizer_muon_gb300", "csrc")
+    for f in NS5_SOURCES:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def parse():
@@ -327,6 +344,8 @@ def run_ours(args, torch):
     peak_tc = pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
     peak_hbm = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
     n_ns5_launches = 15 * max(1, math.ceil(len(wl.shape_groups()) / 8))
+    tr = NS5_TRAFFIC.get(wl.key)
+    ns5_traffic = tr["bytes_per_launch"] if tr and tr["sources"] == ns5_sources_hash() else None
 
     line = {
         "metric": METRIC, "value": round(period_ms / wl.K, 4), "unit": "ms", "n_gpus": world,
@@ -343,7 +362,9 @@ def run_ours(args, torch):
         "rownorm_gbs": round(rn_gbs, 1),
         "roofline": {"kernel": "ns_tc_kernel (Newton-Schulz GEMMs)", "bound": "tensor",
                      "achieved": round(ns5_tflops, 1), "peak": peak_tc, "unit": "TFLOP/s",
-                     "frac": round(ns5_tflops / peak_tc, 4), "traffic": None,
+                     "frac": round(ns5_tflops / peak_tc, 4), "traffic": ns5_traffic,
+                     "achieved_executed": round(ns5_exec_tflops, 1),
+                     "frac_executed": round(ns5_exec_tflops / peak_tc, 4),
                      "peak_source": f"{pk_src} bf16_tflops_sustained",
                      "frac_of_nominal_2250": round(ns5_tflops / 2250.0, 4),
                      "flops_per_refresh": flops, "launches_per_refresh": n_ns5_launches},

@@ -140,3 +140,56 @@ def test_mmdit_1_3b_rownorm_invariants_all_matrices():
         u = -w.double() / (0.15 * 0.2 * max(a, b) ** 0.5)
         norms = u.norm(dim=1 if a <= b else 0)
         assert torch.allclose(norms, torch.ones_like(norms), atol=1e-5), (a, b)
+
+
+def _sampled_period(wl_key, sample_shapes, seed, steps=3):
+    """All matrices of the set on the GPU for `steps` steps; the first matrix of each
+    shape in `sample_shapes` is checked against the oracle every step."""
+    wl = WORKLOADS[wl_key]
+    shapes = [(m.rows, m.cols) for m in wl.matrices]
+    d = dev()
+    torch.cuda.empty_cache()
+    W = [weight_init_torch(torch, d, a, b, seed, i, torch.bfloat16) for i, (a, b) in enumerate(shapes)]
+    M = [torch.zeros(s, device=d) for s in shapes]
+    ws = mm.alloc_workspace(shapes)
+    sample = {}
+    for i, s in enumerate(shapes):
+        if s in sample_shapes:
+            sample.setdefault(s, i)
+    sample = sorted(sample.values())
+    refW = {i: to_np(W[i]) for i in sample}
+    refM = {i: np.zeros(shapes[i]) for i in sample}
+    G = [torch.empty(s, device=d, dtype=torch.bfloat16) for s in shapes]
+    for t in range(steps):
+        for i, (a, b) in enumerate(shapes):
+            gradient_torch(torch, d, a, b, wl.spike_scales, seed, i, t, torch.bfloat16, out=G[i])
+        Gn = {i: to_np(G[i]) for i in sample}
+        for i in sample:
+            W[i].copy_(torch.from_numpy(refW[i].astype(np.float32)).to(d, torch.bfloat16))
+        br = mm.muon_periodic_step(W, G, M, t, ws)
+        torch.cuda.synchronize()
+        for i in sample:
+            prevW = refW[i]
+            refW[i], refM[i], refresh = muon_ref.periodic_step(refW[i], refM[i], Gn[i], t, w_dtype="bf16")
+            assert br == int(refresh)
+            assert_f32_close(to_np(M[i]), refM[i], what=f"M {shapes[i]} step {t}")
+            check_step_w(to_np(W[i]), refW[i], prevW, refresh, "bf16", "bf16", refM[i])
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+    del W, M, G, ws
+    torch.cuda.empty_cache()
+
+
+def test_mmdit_4b_full_set_sampled():
+    """4B MMDiT set (170 matrices, H=2560): one K=3 period, square and tall 6H x H sampled."""
+    H = 2560
+    _sampled_period("mmdit-4b", {(H, H), (6 * H, H), (H, 4 * H)}, seed=91)
+
+
+def test_mmdit_15b_full_set_sampled():
+    """15B MMDiT set (440 matrices, H=3072, about 240 GB with the workspace): one
+    refresh and one RowNorm step, square and tall 3H x H sampled."""
+    H = 3072
+    free, total = torch.cuda.mem_get_info()
+    if free < 250e9:
+        pytest.skip(f"needs ~250 GB free, {free / 1e9:.0f} GB available")
+    _sampled_period("mmdit-15b", {(H, H), (3 * H, H)}, seed=92, steps=2)
