@@ -151,8 +151,11 @@ int muon_apply(const muon_matrix* mats, int n, const void* const* U, int u_dtype
  *   U = NS5(M) (refresh) or RowNorm(M) (otherwise);
  *   W <- W - eta*(s*U + lambda*W), s = 0.2*sqrt(max(A, B)), times gamma when not refreshing.
  * On refresh steps the apply is fused into the last Newton-Schulz GEMM; on
- * RowNorm steps momentum, normalisation and apply are one pass over memory for
- * wide matrices and two passes for tall ones.  branch_out (host, optional)
+ * RowNorm steps momentum, normalisation and apply are one pass over memory
+ * (tall matrices whose strips do not fit the cluster kernel take two passes).
+ * The wide-row kernels of a RowNorm step run on a second stream owned by the
+ * library (one per host thread and device), forked from and joined back to
+ * `stream` with events, so the call stays ordered on `stream` and capturable.  branch_out (host, optional)
  * receives MUON_BRANCH_NS5 or MUON_BRANCH_ROWNORM. */
 int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, float gamma,
                        float mu, float eta, float lambda, int ns5_mode, void* ws,
@@ -192,8 +195,10 @@ int muon_abi_version(void);
  * nothing, so that its consumers' bounded waits expire and report
  * MUON_ERR_TIMEOUT through muon_check_status (no fault, no hang).
  * MUON_DEBUG_NO_CLUSTER sends tall matrices of RowNorm steps through the
- * two-pass kernels instead of the single-pass cluster kernel (to test both). */
-enum { MUON_DEBUG_STALL_PRODUCER = 1, MUON_DEBUG_NO_CLUSTER = 2 };
+ * two-pass kernels instead of the single-pass cluster kernel (to test both).
+ * MUON_DEBUG_NO_OVERLAP runs the wide-row and tall-column kernels of a RowNorm
+ * step one after the other on the caller's stream instead of side by side. */
+enum { MUON_DEBUG_STALL_PRODUCER = 1, MUON_DEBUG_NO_CLUSTER = 2, MUON_DEBUG_NO_OVERLAP = 4 };
 int muon_debug_set(int flags, int timeout_ms);
 
 #ifdef __cplusplus

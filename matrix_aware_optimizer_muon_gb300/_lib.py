@@ -31,6 +31,7 @@ MUON_BRANCH_ROWNORM = 0
 MUON_BRANCH_NS5 = 1
 MUON_DEBUG_STALL_PRODUCER = 1
 MUON_DEBUG_NO_CLUSTER = 2
+MUON_DEBUG_NO_OVERLAP = 4
 
 _NS5_MODES = {"bf16": MUON_NS5_BF16, "f32": MUON_NS5_F32}
 

@@ -186,6 +186,30 @@ int check_ws(const Plan& P, void* ws, size_t ws_bytes) {
   return MUON_OK;
 }
 
+// A second stream per (host thread, device) for running independent kernels of one
+// step side by side, with the events that fork it from and join it back to the
+// caller's stream.  Created on first use; they are not device memory.
+struct AuxStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+AuxStream* aux_stream() {
+  static thread_local std::map<int, AuxStream> per_device;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  AuxStream& a = per_device[dev];
+  if (!a.stream) {
+    if (cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) {
+      a = AuxStream{};
+      return nullptr;
+    }
+  }
+  return &a;
+}
+
 int cuda_status(cudaError_t e) {
   if (e != cudaSuccess) return MUON_ERR_CUDA;
   ++t_launches;
@@ -730,6 +754,19 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
     if (mats[i].rows <= mats[i].cols && mats[i].cols <= ROWS_MAX_COLS) rows_by_cols[(int)mats[i].cols].push_back(i);
     else two_pass.push_back(i);
   }
+  // Wide rows and tall columns are independent: when both are present the rows
+  // kernels run on a second stream next to the tall-matrix kernels, so that
+  // one kernel's CTAs stream while the other's wait on their line reductions.
+  cudaStream_t rs = s;
+  AuxStream* aux = nullptr;
+  if (!rows_by_cols.empty() && !two_pass.empty() && !(g_debug_flags.load() & MUON_DEBUG_NO_OVERLAP)) {
+    aux = aux_stream();
+    if (aux) {
+      if (cudaEventRecord(aux->fork, s) != cudaSuccess || cudaStreamWaitEvent(aux->stream, aux->fork, 0) != cudaSuccess)
+        return MUON_ERR_CUDA;
+      rs = aux->stream;
+    }
+  }
   static thread_local RowsParams rp;
   for (const auto& kv : rows_by_cols) {
     const std::vector<int>& v = kv.second;
@@ -757,7 +794,7 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
       }
       rp.nmat = j;
       rp.total_rows = rows;
-      if ((rc = cuda_status(launch_rows(ck.w_dt, ck.g_dt, kv.first, rp, s))) != MUON_OK) return rc;
+      if ((rc = cuda_status(launch_rows(ck.w_dt, ck.g_dt, kv.first, rp, rs))) != MUON_OK) return rc;
     }
   }
   // tall matrices: single pass, one thread-block cluster per column strip
@@ -825,6 +862,10 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
     if (rc != MUON_OK) return rc;
     rc = run_ew(mats, two_pass, EW_APPLY_LINE, ck.w_dt, ck.g_dt, MUON_DTYPE_F32, mu, eta, lambda, fill, s);
     if (rc != MUON_OK) return rc;
+  }
+  if (aux) {
+    if (cudaEventRecord(aux->join, aux->stream) != cudaSuccess || cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess)
+      return MUON_ERR_CUDA;
   }
   prof_record(4, s);
   return MUON_OK;
