@@ -32,7 +32,9 @@ Readings where the pages are silent (each also listed in the design doc):
   with no epsilon;
 * the NS5 iteration runs on the short side: a tall matrix is transposed, iterated,
   and transposed back;
-* bf16 storage of W is round-to-nearest-even of the exact fp64 result.
+* bf16 storage of W is round-to-nearest-even of the exact fp64 result;
+* the Eq. (6) "Update Norm" variant on RowNorm steps takes the RMS over the lines
+  that carry the update, i.e. it equals the Eq. (7) scale unless a line is zero.
 
 Every function here is pinned by the tests in tests/test_oracle_pins.py against
 closed forms, invariants, values the pages print, or brute force.  No function
@@ -154,6 +156,38 @@ def round_to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(dtype)
 
 
+SCALE_ADJUSTED_LR = "adjusted_lr"   # Eq. (4)/(7): 0.2*sqrt(max(A, B))
+SCALE_UPDATE_NORM = "update_norm"   # Eq. (6): 0.2/RMS(U)
+
+
+def update_norm_scale(U: np.ndarray, refresh: bool, gamma: float) -> float:
+    """Muon is Scalable for LLM Training, section 3.1, Eq. (6): the update is normalised
+    to RMS 0.2 exactly, s = 0.2/RMS(U) (times gamma on RowNorm steps).
+
+    Reading for the RowNorm branch: the RMS is taken over the lines that carry the
+    update (a zero line carries none), so each unit line of length m gives RMS
+    1/sqrt(m).  A zero direction gives s = 0.
+    """
+    U = np.asarray(U, dtype=np.float64)
+    A, B = U.shape
+    if refresh:
+        r = rms(U)
+    else:
+        line_axis = 1 if B >= A else 0
+        nz = int(np.count_nonzero(np.sqrt(np.sum(U * U, axis=line_axis)) > 0.0))
+        r = math.sqrt(float(np.sum(U * U)) / (nz * max(A, B))) if nz else 0.0
+    if r == 0.0:
+        return 0.0
+    s = RMS_MATCH / r
+    return s * gamma if not refresh else s
+
+
+def update_rms(U: np.ndarray) -> float:
+    """Update-RMS telemetry (Muon is Scalable, section 2.2, the monitoring after Lemma 1):
+    RMS of the direction before scaling, over all A*B elements."""
+    return rms(U)
+
+
 def muon_direction(M: np.ndarray, refresh: bool) -> np.ndarray:
     """U_t: Newton-Schulz on refresh steps, RowNorm otherwise."""
     return newton_schulz(M) if refresh else rownorm(M)
@@ -161,7 +195,8 @@ def muon_direction(M: np.ndarray, refresh: bool) -> np.ndarray:
 
 def periodic_step(W: np.ndarray, M_prev: np.ndarray, G: np.ndarray, step: int, K: int = K_DEFAULT,
                   gamma: float = GAMMA_DEFAULT, mu: float = MU_DEFAULT, eta: float = 0.02,
-                  lam: float = 0.01, w_dtype: str = "f64"):
+                  lam: float = 0.01, w_dtype: str = "f64", scale_mode: str = SCALE_ADJUSTED_LR,
+                  telemetry: bool = False):
     """One Periodic Row-wise Muon step on one matrix; returns (W_new, M_new, refresh).
 
     Order: momentum (Eq. (1)), branch choice (step % K), direction (Eq. (2) or RowNorm),
@@ -172,7 +207,15 @@ def periodic_step(W: np.ndarray, M_prev: np.ndarray, G: np.ndarray, step: int, K
     M = momentum(M_prev, G, mu)
     refresh = is_refresh(step, K)
     U = muon_direction(M, refresh)
-    W_new = apply_update(W, U, update_scale(A, B, refresh, gamma), eta, lam)
+    if scale_mode == SCALE_ADJUSTED_LR:
+        scale = update_scale(A, B, refresh, gamma)
+    elif scale_mode == SCALE_UPDATE_NORM:
+        scale = update_norm_scale(U, refresh, gamma)
+    else:
+        raise ValueError(scale_mode)
+    W_new = apply_update(W, U, scale, eta, lam)
+    if telemetry:
+        return round_to_storage(W_new, w_dtype), M, refresh, update_rms(U)
     return round_to_storage(W_new, w_dtype), M, refresh
 
 

@@ -284,10 +284,61 @@ def check_bf16_rounding(o):
     assert np.array_equal(o.round_to_storage(x.astype(np.float64), "bf16"), want)
 
 
+def check_update_norm(o):
+    """Eq. (6): the applied direction has RMS exactly 0.2 (0.2*gamma on RowNorm steps),
+    is a positive multiple of U, and on RowNorm steps without zero lines it equals Eq. (7)."""
+    rng = np.random.default_rng(13)
+    for (A, B) in [(12, 30), (30, 12), (16, 16)]:
+        M = rng.standard_normal((A, B))
+        O = o.newton_schulz(M)
+        s = o.update_norm_scale(O, True, 0.15)
+        assert abs(math.sqrt(float(np.mean((s * O) ** 2))) - 0.2) < 1e-12
+        assert s > 0
+        R = o.rownorm(M)
+        s_r = o.update_norm_scale(R, False, 0.15)
+        assert abs(s_r - 0.15 * 0.2 * math.sqrt(max(A, B))) < 1e-12
+        W = rng.standard_normal((A, B))
+        a = o.periodic_step(W, np.zeros((A, B)), M, 1, 3, scale_mode="update_norm")
+        b = o.periodic_step(W, np.zeros((A, B)), M, 1, 3, scale_mode="adjusted_lr")
+        assert np.max(np.abs(a[0] - b[0])) < 1e-12
+        # refresh step: brute force W - eta*(0.2*O/RMS(O) + lam*W)
+        c = o.periodic_step(W, np.zeros((A, B)), M, 0, 3, scale_mode="update_norm")
+        r = math.sqrt(sum(O[i][j] ** 2 for i in range(A) for j in range(B)) / (A * B))
+        for i in range(A):
+            for j in range(B):
+                assert abs(c[0][i][j] - (W[i][j] - 0.02 * (0.2 * O[i][j] / r + 0.01 * W[i][j]))) < 1e-12
+    # a zero line carries no update; the RMS is over the remaining lines
+    M = rng.standard_normal((5, 9))
+    M[2, :] = 0.0
+    R = o.rownorm(M)
+    assert abs(o.update_norm_scale(R, False, 1.0) - 0.2 * 3.0) < 1e-12
+    assert o.update_norm_scale(np.zeros((3, 4)), True, 0.15) == 0.0
+
+
+def check_update_rms(o):
+    rng = np.random.default_rng(14)
+    for (A, B) in [(6, 11), (11, 6)]:
+        M = rng.standard_normal((A, B))
+        if A <= B:
+            M[0, :] = 0.0
+        else:
+            M[:, 0] = 0.0
+        R = o.rownorm(M)
+        n_nz = min(A, B) - 1
+        assert abs(o.update_rms(R) - math.sqrt(n_nz / (A * B))) < 1e-12
+        W = rng.standard_normal((A, B))
+        out = o.periodic_step(W, np.zeros((A, B)), M, 1, 3, telemetry=True)
+        assert abs(out[3] - math.sqrt(n_nz / (A * B))) < 1e-12
+        out = o.periodic_step(W, np.zeros((A, B)), M, 0, 3, telemetry=True)
+        Uo = o.newton_schulz(M)
+        assert abs(out[3] - math.sqrt(sum(Uo[i][j] ** 2 for i in range(A) for j in range(B)) / (A * B))) < 1e-12
+
+
 ALL_CHECKS = [check_constants, check_ns5_closed_form, check_ns5_diagonal, check_ns5_orthogonal_input,
               check_ns5_polar_and_band, check_ns5_short_side, check_ns5_scale_and_zero,
               check_rownorm_bruteforce, check_rownorm_invariants, check_lemma1, check_momentum,
-              check_apply, check_scale, check_schedule, check_step, check_bf16_rounding]
+              check_apply, check_scale, check_schedule, check_step, check_bf16_rounding, check_update_norm,
+              check_update_rms]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
@@ -331,6 +382,9 @@ MUTATIONS = [
     ("return step % K == 0", "return step % K == K - 1"),
     ("q = np.rint(np.ldexp(frac, 8))", "q = np.floor(np.ldexp(frac, 8) + 0.5)"),
     ("U = muon_direction(M, refresh)", "U = muon_direction(M_prev, refresh)"),
+    ("    s = RMS_MATCH / r\n", "    s = RMS_MATCH * r\n"),
+    ("nz = int(np.count_nonzero(np.sqrt(np.sum(U * U, axis=line_axis)) > 0.0))", "nz = min(A, B)"),
+    ("        r = rms(U)\n", "        r = math.sqrt(float(np.mean(np.abs(U))))\n"),
 ]
 
 
