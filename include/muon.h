@@ -166,6 +166,30 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
  * already zero; the rest of the workspace needs no initialisation. */
 int muon_workspace_init(void* ws, size_t ws_bytes, muon_stream_t stream);
 
+/* Update scale of muon_periodic_step_ex. */
+enum {
+  MUON_SCALE_ADJUSTED_LR = 0, /* s = 0.2*sqrt(max(A, B)) ("Muon is Scalable" notes, Eq. (4)/(7)) */
+  MUON_SCALE_UPDATE_NORM = 1  /* s = 0.2/RMS(U), "Update Norm", same notes, section 3.1, Eq. (6);
+                                 on RowNorm steps the RMS is over the lines that carry the update,
+                                 so it equals the Eq. (7) scale unless a line of M is zero */
+};
+
+typedef struct muon_step_options {
+  int scale_mode;      /* MUON_SCALE_* */
+  float* update_rms;   /* optional device array of n floats: RMS of each matrix's direction U
+                          (the Newton-Schulz output, or the RowNorm of M) over its A*B elements,
+                          as monitored against Lemma 1 ("Muon is Scalable" notes, section 2.2) */
+} muon_step_options;
+
+/* muon_periodic_step with options (opts == NULL: Eq. (4)/(7) scale, no telemetry).
+ * With MUON_SCALE_UPDATE_NORM, refresh steps write O to the workspace, reduce its
+ * sum of squares in a fixed order, then apply W <- W - eta*(0.2*O/RMS(O) + lambda*W)
+ * in a separate pass (a zero O gives pure weight decay). */
+int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, float gamma,
+                          float mu, float eta, float lambda, int ns5_mode,
+                          const muon_step_options* opts, void* ws, size_t ws_bytes,
+                          muon_stream_t stream, int* branch_out);
+
 /* Synchronises `stream`, reads and clears the device status word in `ws`, and
  * returns MUON_OK or the recorded error (MUON_ERR_TIMEOUT). */
 int muon_check_status(void* ws, size_t ws_bytes, muon_stream_t stream);

@@ -42,6 +42,15 @@ class MuonError(RuntimeError):
         super().__init__(f"{fn} failed: {status} ({status_str(status)})")
 
 
+MUON_SCALE_ADJUSTED_LR = 0
+MUON_SCALE_UPDATE_NORM = 1
+_SCALE_MODES = {"adjusted_lr": MUON_SCALE_ADJUSTED_LR, "update_norm": MUON_SCALE_UPDATE_NORM}
+
+
+class MuonStepOptions(ctypes.Structure):
+    _fields_ = [("scale_mode", ctypes.c_int), ("update_rms", ctypes.c_void_p)]
+
+
 class MuonMatrix(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("G", ctypes.c_void_p), ("M", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
@@ -72,6 +81,9 @@ def load_library(path: Optional[str] = None):
         "muon_apply": (i32, [mp, i32, ptrs, i32, f32, f32, f32, vp]),
         "muon_periodic_step": (i32, [mp, i32, i64, i32, f32, f32, f32, f32, i32, vp, sz, vp,
                                      ctypes.POINTER(ctypes.c_int)]),
+        "muon_periodic_step_ex": (i32, [mp, i32, i64, i32, f32, f32, f32, f32, i32,
+                                        ctypes.POINTER(MuonStepOptions), vp, sz, vp,
+                                        ctypes.POINTER(ctypes.c_int)]),
         "muon_workspace_init": (i32, [vp, sz, vp]),
         "muon_check_status": (i32, [vp, sz, vp]),
         "muon_status_str": (ctypes.c_char_p, [i32]),
@@ -238,12 +250,22 @@ def muon_apply(W: Sequence[torch.Tensor], U: Sequence[torch.Tensor], scale_mul: 
 
 def muon_periodic_step(W: Sequence[torch.Tensor], G: Sequence[torch.Tensor], M: Sequence[torch.Tensor],
                        step: int, ws: torch.Tensor, K: int = 3, gamma: float = 0.15, mu: float = 0.95,
-                       eta: float = 0.02, lam: float = 0.01, ns5_mode: str = "bf16", stream=None) -> int:
+                       eta: float = 0.02, lam: float = 0.01, ns5_mode: str = "bf16", stream=None,
+                       scale_mode: str = "adjusted_lr", update_rms: Optional[torch.Tensor] = None) -> int:
+    """One Periodic Row-wise Muon step; returns MUON_BRANCH_NS5 or MUON_BRANCH_ROWNORM.
+    scale_mode "update_norm" selects Eq. (6); update_rms (n fp32 on the device) receives
+    the RMS of each matrix's direction."""
     arr, n = make_matrices(M, W, G)
     br = ctypes.c_int(-1)
-    _check("muon_periodic_step", load_library().muon_periodic_step(
-        arr, n, int(step), int(K), gamma, mu, eta, lam, _NS5_MODES[ns5_mode], _ptr(ws), ws.numel(),
-        _stream(stream), ctypes.byref(br)))
+    lib = load_library()
+    if scale_mode == "adjusted_lr" and update_rms is None:
+        st = lib.muon_periodic_step(arr, n, int(step), int(K), gamma, mu, eta, lam, _NS5_MODES[ns5_mode],
+                                    _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(br))
+    else:
+        opts = MuonStepOptions(_SCALE_MODES[scale_mode], _ptr(update_rms))
+        st = lib.muon_periodic_step_ex(arr, n, int(step), int(K), gamma, mu, eta, lam, _NS5_MODES[ns5_mode],
+                                       ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(br))
+    _check("muon_periodic_step", st)
     return br.value
 
 

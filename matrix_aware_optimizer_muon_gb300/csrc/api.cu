@@ -107,7 +107,7 @@ bool make_plan(const muon_matrix* mats, int n, int ns5_mode, Plan* P) {
   P->groups.clear();
   P->ns5_mode = ns5_mode;
   const size_t esize = ns5_mode == MUON_NS5_F32 ? 4 : 2;
-  size_t fro_floats = 0, line_floats = 0, inv_floats = 0;
+  size_t fro_floats = 0, line_floats = 0, inv_floats = 0, osq_floats = 0;
   std::map<std::pair<int, int>, std::vector<int>> open;  // (n, m) -> current group indices
   for (int i = 0; i < n; ++i) {
     MatPlan& mp = P->mats[i];
@@ -127,6 +127,9 @@ bool make_plan(const muon_matrix* mats, int n, int ns5_mode, Plan* P) {
     line_floats += (size_t)mp.line_tiles * mp.lines;
     mp.line_inv = inv_floats;
     inv_floats += mp.lines;
+    // O^2 partials of the last UPDATE: [128x256 tile][8 epilogue warps] or [64x64 tile]
+    mp.osq = osq_floats;
+    osq_floats += std::max((size_t)cdiv(mp.n, 128) * cdiv(mp.m, 256) * 8, (size_t)cdiv(mp.n, 64) * cdiv(mp.m, 64));
     // shape groups of at most NS_MAX_MATS matrices, first-appearance order
     const auto key = std::make_pair(mp.n, mp.m);
     int gi = -1;
@@ -160,6 +163,12 @@ bool make_plan(const muon_matrix* mats, int n, int ns5_mode, Plan* P) {
   off = align_up(off + line_floats * 4, kAlign);
   P->line_inv = off;
   off = align_up(off + inv_floats * 4, kAlign);
+  P->osq_part = off;
+  off = align_up(off + osq_floats * 4, kAlign);
+  P->scale = off;
+  off = align_up(off + (size_t)std::max(n, 1) * 4, kAlign);
+  P->nz = off;
+  off = align_up(off + (size_t)std::max(n, 1) * 4, kAlign);
   for (GroupPlan& g : P->groups) {
     const size_t xb = (size_t)g.count * g.n * g.ld_m * esize;
     const size_t sb = (size_t)g.count * g.n * g.ld_n * esize;
@@ -288,7 +297,7 @@ int run_fro_final(const Plan& P, uint8_t* ws, const std::vector<int>& idx, const
   return MUON_OK;
 }
 
-int run_line_final(const Plan& P, uint8_t* ws, const std::vector<int>& idx, cudaStream_t s) {
+int run_line_final(const Plan& P, uint8_t* ws, const std::vector<int>& idx, cudaStream_t s, int* nz = nullptr) {
   static thread_local LineFinalParams prm;
   size_t k = 0;
   while (k < idx.size()) {
@@ -300,6 +309,7 @@ int run_line_final(const Plan& P, uint8_t* ws, const std::vector<int>& idx, cuda
       LineFinalMat& e = prm.mat[j++];
       e.part = reinterpret_cast<const float*>(ws + P.line_part) + mp.line_part;
       e.inv = reinterpret_cast<float*>(ws + P.line_inv) + mp.line_inv;
+      e.nz = nz ? nz + idx[k] : nullptr;
       e.parts = mp.line_tiles;
       e.lines = mp.lines;
       e.line_begin = lines;
@@ -329,8 +339,15 @@ struct GroupMaps {
   CUtensorMap x128[2], x256[2], x64[2], s128, s256, b128;
 };
 
+// Partials of sum(O^2) written by the last UPDATE: where each matrix's lie.
+struct OsqLayout {
+  std::vector<long long> begin;  // list order
+  std::vector<int> count;
+};
+
 int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, int dst_dtype,
-            void* const* dst_ptrs /* list order */, float eta, float lam, int sms, cudaStream_t s) {
+            void* const* dst_ptrs /* list order */, float eta, float lam, int sms, cudaStream_t s,
+            OsqLayout* osq = nullptr) {
   const bool tcmode = P.ns5_mode == MUON_NS5_BF16;
   const size_t esize = tcmode ? 2 : 4;
   const int ng = (int)P.groups.size();
@@ -373,6 +390,12 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
   std::vector<int> gbase(ng + 1, 0);
   for (int gi = 0; gi < ng; ++gi) gbase[gi + 1] = gbase[gi] + P.groups[gi].count;
   const float* inv_norm_all = reinterpret_cast<const float*>(ws + P.inv_norm);
+  const int slots = tcmode ? 8 : 1;   // O^2 partials per tile: one per epilogue warp, or one per CTA
+  long long osq_off = 0;
+  if (osq) {
+    osq->begin.assign(P.mats.size(), 0);
+    osq->count.assign(P.mats.size(), 0);
+  }
   static thread_local NsParams prm;
   for (int iter = 0; iter < kNsSteps; ++iter) {
     const int cur = iter & 1;
@@ -437,6 +460,8 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
               // and reads the residual of X_k when 1 <= k <= NS_LO_ITERS
               if (iter < NS_LO_ITERS && iter + 1 < kNsSteps) G.lo_out = ws + ((iter & 1) ? g.lo1 : g.lo0);
               if (iter >= 1 && iter <= NS_LO_ITERS) G.lo_in = ws + (((iter - 1) & 1) ? g.lo1 : g.lo0);
+              // O kept in the workspace (Eq. (6)): its bf16 residual goes to lo0
+              if (dst_mode == 2 && iter == kNsSteps - 1) G.lo_out = ws + g.lo0;
             }
             if (tcmode) { G.mapA = maps[gi].b128; G.mapB = maps[gi].x64[cur]; }
           }
@@ -471,6 +496,18 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
           mbase += g.count;
         }
         prm.total_tiles = tiles;
+        if (osq && prm.last_iter) {
+          prm.osq_part = reinterpret_cast<float*>(ws + P.osq_part) + osq_off;
+          for (int gi = ch.first; gi < ch.second; ++gi) {
+            const NsGroup& G = prm.g[gi - ch.first];
+            for (int q = 0; q < G.count; ++q) {
+              const int li = P.groups[gi].mats[q];
+              osq->begin[li] = osq_off + (long long)(G.tile_begin + q * G.tiles_per_mat) * slots;
+              osq->count[li] = G.tiles_per_mat * slots;
+            }
+          }
+          osq_off += (long long)tiles * slots;
+        }
         const cudaError_t e = tcmode ? launch_ns_tc(prm, s, sms) : launch_ns_simt(prm, s);
         if (cuda_status(e) != MUON_OK) return MUON_ERR_CUDA;
       }
@@ -714,9 +751,20 @@ int muon_apply(const muon_matrix* mats, int n, const void* const* U, int u_dtype
 int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, float gamma, float mu, float eta,
                        float lambda, int ns5_mode, void* ws, size_t ws_bytes, muon_stream_t stream,
                        int* branch_out) {
+  return muon_periodic_step_ex(mats, n, step, K, gamma, mu, eta, lambda, ns5_mode, nullptr, ws, ws_bytes, stream,
+                               branch_out);
+}
+
+int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, float gamma, float mu, float eta,
+                          float lambda, int ns5_mode, const muon_step_options* opts, void* ws, size_t ws_bytes,
+                          muon_stream_t stream, int* branch_out) {
   t_launches = 0;
   if (K < 1 || step < 0) return MUON_ERR_INVALID;
   if (ns5_mode != MUON_NS5_BF16 && ns5_mode != MUON_NS5_F32) return MUON_ERR_UNSUPPORTED;
+  const int scale_mode = opts ? opts->scale_mode : MUON_SCALE_ADJUSTED_LR;
+  float* update_rms = opts ? opts->update_rms : nullptr;
+  if (scale_mode != MUON_SCALE_ADJUSTED_LR && scale_mode != MUON_SCALE_UPDATE_NORM) return MUON_ERR_UNSUPPORTED;
+  if (update_rms && !aligned(update_rms, 4)) return MUON_ERR_INVALID;
   Check ck;
   t_launches = 0;
   int rc = validate(mats, n, true, true, true, &ck);
@@ -740,11 +788,77 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
     std::vector<void*> dst(n);
     for (int i = 0; i < n; ++i) dst[i] = mats[i].W;
     prof_record(1, s);
-    rc = run_ns5(P, mats, w, 1, ck.w_dt, dst.data(), eta, lambda, di.sms, s);
+    OsqLayout osq;
+    const bool norm = scale_mode == MUON_SCALE_UPDATE_NORM;
+    const bool want_osq = norm || update_rms;
+    // Eq. (4)/(7): the apply is fused into the last UPDATE.  Eq. (6): O stays in
+    // the workspace until its RMS is known, then a separate pass applies it.
+    rc = run_ns5(P, mats, w, norm ? 2 : 1, ck.w_dt, dst.data(), eta, lambda, di.sms, s, want_osq ? &osq : nullptr);
+    if (rc != MUON_OK) return rc;
+    if (want_osq) {
+      float* scale = reinterpret_cast<float*>(w + P.scale);
+      static thread_local OsqFinalParams fp;
+      int i = 0;
+      while (i < n) {
+        std::memset(&fp, 0, sizeof(fp));
+        fp.part = reinterpret_cast<const float*>(w + P.osq_part);
+        fp.rms_out = update_rms;
+        fp.scale_out = norm ? scale : nullptr;
+        fp.rms_match = kRmsMatch;
+        int j = 0;
+        for (; i < n && j < FIN_MAX_MATS; ++i, ++j) {
+          fp.begin[j] = osq.begin[i];
+          fp.count[j] = osq.count[i];
+          fp.out_index[j] = i;
+          fp.numel[j] = (double)mats[i].rows * (double)mats[i].cols;
+        }
+        fp.nmat = j;
+        if ((rc = cuda_status(launch_osq_final(fp, s))) != MUON_OK) return rc;
+      }
+      if (norm) {
+        const bool tc = ns5_mode == MUON_NS5_BF16;
+        const size_t esize = tc ? 2 : 4;
+        static thread_local ApplyWsParams ap;
+        int k = 0;
+        while (k < n) {
+          std::memset(&ap, 0, sizeof(ap));
+          ap.scale = scale;
+          ap.eta = eta;
+          ap.lam = lambda;
+          int j = 0, tiles = 0;
+          for (; k < n && j < APPLYWS_MAX_MATS; ++k) {
+            if (!nonempty(mats[k])) continue;
+            const MatPlan& mp = P.mats[k];
+            const GroupPlan& g = P.groups[mp.group];
+            ApplyWsMat& e = ap.mat[j++];
+            const size_t moff = (size_t)mp.idx_in_group * g.n * g.ld_m;
+            e.W = mats[k].W;
+            e.O = w + g.x1 + moff * esize;                       // output of the last UPDATE
+            e.O_lo = tc ? (const void*)(w + g.lo0 + moff * 2) : nullptr;
+            e.n = g.n;
+            e.m = g.m;
+            e.ld = g.ld_m;
+            e.tall = mp.tall;
+            e.tiles_c = cdiv(g.m, APPLYWS_TILE);
+            e.tile_begin = tiles;
+            e.scale_index = k;
+            tiles += cdiv(g.n, APPLYWS_TILE) * e.tiles_c;
+          }
+          ap.nmat = j;
+          ap.total_tiles = tiles;
+          if (j > 0 && (rc = cuda_status(launch_apply_ws(ck.w_dt, tc ? MUON_DTYPE_BF16 : MUON_DTYPE_F32, ap, s))) !=
+                           MUON_OK)
+            return rc;
+        }
+      }
+    }
     prof_record(2, s);
-    return rc;
+    return MUON_OK;
   }
   prof_record(3, s);
+  // Update-RMS telemetry of a RowNorm step: count the nonzero lines.
+  int* nz = update_rms ? reinterpret_cast<int*>(w + P.nz) : nullptr;
+  if (nz && cudaMemsetAsync(nz, 0, sizeof(int) * (size_t)n, s) != cudaSuccess) return MUON_ERR_CUDA;
 
   // RowNorm branch: s = gamma * 0.2 * sqrt(max(A, B))
   std::vector<int> two_pass;
@@ -783,6 +897,7 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
         e.W = a.W;
         e.G = a.G;
         e.M = a.M;
+        e.nz = nz ? nz + v[k] : nullptr;
         e.rows = (int)a.rows;
         e.cols = (int)a.cols;
         e.row_begin = rows;
@@ -828,6 +943,7 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
           e.W = a.W;
           e.G = a.G;
           e.M = a.M;
+          e.nz = nz ? nz + v[k] : nullptr;
           e.rows = (int)a.rows;
           e.cols = (int)a.cols;
           e.unit_begin = units;
@@ -858,7 +974,7 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
     rc = run_ew(mats, two_pass, EW_MOMENTUM | EW_LINEPART, ck.w_dt, ck.g_dt, MUON_DTYPE_F32, mu, eta, lambda,
                 fill, s);
     if (rc != MUON_OK) return rc;
-    rc = run_line_final(P, w, two_pass, s);
+    rc = run_line_final(P, w, two_pass, s, nz);
     if (rc != MUON_OK) return rc;
     rc = run_ew(mats, two_pass, EW_APPLY_LINE, ck.w_dt, ck.g_dt, MUON_DTYPE_F32, mu, eta, lambda, fill, s);
     if (rc != MUON_OK) return rc;
@@ -866,6 +982,22 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
   if (aux) {
     if (cudaEventRecord(aux->join, aux->stream) != cudaSuccess || cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess)
       return MUON_ERR_CUDA;
+  }
+  if (nz) {
+    static thread_local NzRmsParams zp;
+    int i = 0;
+    while (i < n) {
+      std::memset(&zp, 0, sizeof(zp));
+      zp.nz = nz;
+      zp.rms_out = update_rms;
+      int j = 0;
+      for (; i < n && j < FIN_MAX_MATS; ++i, ++j) {
+        zp.out_index[j] = i;
+        zp.numel[j] = (double)mats[i].rows * (double)mats[i].cols;
+      }
+      zp.nmat = j;
+      if ((rc = cuda_status(launch_nz_rms(zp, s))) != MUON_OK) return rc;
+    }
   }
   prof_record(4, s);
   return MUON_OK;

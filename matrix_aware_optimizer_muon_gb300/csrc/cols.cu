@@ -160,6 +160,11 @@ __global__ void __launch_bounds__(NT, 2) cols_cluster_kernel(const __grid_consta
     inv[threadIdx.x] = inv_norm_from_sumsq(t);
   }
   __syncthreads();
+  if (mt.nz && rank == 0 && threadIdx.x < 32) {   // telemetry: nonzero columns of this strip
+    const int c = threadIdx.x;
+    const unsigned nzb = __ballot_sync(0xffffffffu, c < CW && c0 + c < B && inv[c < CW ? c : 0] > 0.f);
+    if (threadIdx.x == 0 && nzb) atomicAdd(mt.nz, __popc(nzb));
+  }
 
   // ---- apply from shared memory
   float iv[4];

@@ -289,6 +289,7 @@ rows_kernel(const __grid_constant__ RowsParams p) {
     for (int j = 0; j < 4; ++j) ss = fmaf(v[k][j], v[k][j], ss);
   }
   const float inv = inv_norm_from_sumsq(block_sum(ss, red));
+  if (mt.nz && threadIdx.x == 0 && inv > 0.f) atomicAdd(mt.nz, 1);   // telemetry: nonzero rows
 #pragma unroll
   for (int k = 0; k < CPT; ++k) {
     const int c = (threadIdx.x + k * blockDim.x) * 4;
@@ -394,7 +395,89 @@ line_final_kernel(const __grid_constant__ LineFinalParams p) {
   const int l = g - mt.line_begin;
   double s = 0.0;
   for (int q = 0; q < mt.parts; ++q) s += (double)mt.part[(size_t)q * mt.lines + l];
-  mt.inv[l] = inv_norm_from_sumsq((float)s);
+  const float inv = inv_norm_from_sumsq((float)s);
+  mt.inv[l] = inv;
+  if (mt.nz && inv > 0.f) atomicAdd(mt.nz, 1);   // telemetry: nonzero lines
+}
+
+// One CTA per matrix: sum of the O^2 partials (fixed order) -> RMS(O) and the
+// Eq. (6) scale rms_match / RMS(O) (zero for a zero output).
+__global__ void __launch_bounds__(256)
+osq_final_kernel(const __grid_constant__ OsqFinalParams p) {
+  __shared__ double red[32];
+  const int i = blockIdx.x;
+  const long long b = p.begin[i];
+  double s = 0.0;
+  for (int t = threadIdx.x; t < p.count[i]; t += blockDim.x) s += (double)p.part[b + t];
+  s = block_sum_f64(s, red);
+  if (threadIdx.x == 0) {
+    const int o = p.out_index[i];
+    const double r = p.numel[i] > 0 ? sqrt(s / p.numel[i]) : 0.0;
+    if (p.rms_out) p.rms_out[o] = (float)r;
+    if (p.scale_out) p.scale_out[o] = r > 0.0 ? (float)(p.rms_match / r) : 0.f;
+  }
+}
+
+// RMS of a RowNorm direction: every nonzero line has unit norm, so RMS^2 = nz / (A*B).
+__global__ void nz_rms_kernel(const __grid_constant__ NzRmsParams p) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= p.nmat) return;
+  const int o = p.out_index[i];
+  p.rms_out[o] = p.numel[i] > 0 ? (float)sqrt((double)p.nz[o] / p.numel[i]) : 0.f;
+}
+
+// W <- W - eta*(scale*O + lambda*W) for O kept in the workspace on the short side
+// (n x m, leading dimension ld).  64 x 64 tiles of O pass through shared memory so
+// that a tall W (m x n, W[c][r] = update of O[r][c]) is read and written along its
+// rows too.
+template <typename WT, typename OT>
+__global__ void __launch_bounds__(256)
+apply_ws_kernel(const __grid_constant__ ApplyWsParams p) {
+  __shared__ float t[APPLYWS_TILE][APPLYWS_TILE + 1];
+  int lo = 0, hi = p.nmat - 1;
+  const int b = blockIdx.x;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.mat[mid].tile_begin <= b) lo = mid; else hi = mid - 1;
+  }
+  const ApplyWsMat& mt = p.mat[lo];
+  const int lt = b - mt.tile_begin;
+  const int tr = lt / mt.tiles_c, tc = lt - tr * mt.tiles_c;
+  const int r0 = tr * APPLYWS_TILE, c0 = tc * APPLYWS_TILE;
+  const int n = mt.n, m = mt.m;
+  const OT* O = reinterpret_cast<const OT*>(mt.O);
+  const bf16* L = reinterpret_cast<const bf16*>(mt.O_lo);
+  for (int idx = threadIdx.x; idx < APPLYWS_TILE * APPLYWS_TILE; idx += blockDim.x) {
+    const int rr = idx / APPLYWS_TILE, cc = idx % APPLYWS_TILE;
+    const int r = r0 + rr, c = c0 + cc;
+    float v = 0.f;
+    if (r < n && c < m) {
+      const size_t off = (size_t)r * mt.ld + c;
+      v = to_f32(O[off]);
+      if (L) v += __bfloat162float(L[off]);
+    }
+    t[rr][cc] = v;
+  }
+  __syncthreads();
+  const float sc = p.scale[mt.scale_index];
+  WT* W = reinterpret_cast<WT*>(mt.W);
+  for (int idx = threadIdx.x; idx < APPLYWS_TILE * APPLYWS_TILE; idx += blockDim.x) {
+    int rr, cc;
+    size_t widx;
+    if (!mt.tall) {          // W is n x m: consecutive threads walk a row of W and of O
+      rr = idx / APPLYWS_TILE;
+      cc = idx % APPLYWS_TILE;
+      widx = (size_t)(r0 + rr) * m + (c0 + cc);
+    } else {                 // W is m x n: consecutive threads walk a row of W (a column of O)
+      cc = idx / APPLYWS_TILE;
+      rr = idx % APPLYWS_TILE;
+      widx = (size_t)(c0 + cc) * n + (r0 + rr);
+    }
+    if (r0 + rr < n && c0 + cc < m) {
+      const float w = ld1(W + widx);
+      st1(W + widx, w - p.eta * (sc * t[rr][cc] + p.lam * w));
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -473,6 +556,28 @@ cudaError_t launch_apply(int w_dt, int u_dt, const ApplyParams& p, cudaStream_t 
 cudaError_t launch_fro_final(const FroFinalParams& p, cudaStream_t s) {
   if (p.nmat <= 0) return cudaSuccess;
   fro_final_kernel<<<p.nmat, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_osq_final(const OsqFinalParams& p, cudaStream_t s) {
+  if (p.nmat <= 0) return cudaSuccess;
+  osq_final_kernel<<<p.nmat, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nz_rms(const NzRmsParams& p, cudaStream_t s) {
+  if (p.nmat <= 0) return cudaSuccess;
+  nz_rms_kernel<<<(p.nmat + 127) / 128, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply_ws(int w_dt, int o_dt, const ApplyWsParams& p, cudaStream_t s) {
+  if (p.total_tiles <= 0) return cudaSuccess;
+  const bool wb = w_dt == MUON_DTYPE_BF16, ob = o_dt == MUON_DTYPE_BF16;
+  if (wb && ob) apply_ws_kernel<bf16, bf16><<<p.total_tiles, 256, 0, s>>>(p);
+  else if (wb && !ob) apply_ws_kernel<bf16, float><<<p.total_tiles, 256, 0, s>>>(p);
+  else if (!wb && ob) apply_ws_kernel<float, bf16><<<p.total_tiles, 256, 0, s>>>(p);
+  else apply_ws_kernel<float, float><<<p.total_tiles, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

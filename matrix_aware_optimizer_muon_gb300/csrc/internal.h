@@ -62,6 +62,7 @@ struct RowsMat {
   void* W;
   const void* G;
   float* M;
+  int* nz;                 // optional: count of nonzero rows (update-RMS telemetry)
   int rows, cols;
   int row_begin;
   float scale;
@@ -83,6 +84,7 @@ struct ColsMat {
   void* W;
   const void* G;
   float* M;
+  int* nz;                 // optional: count of nonzero columns (update-RMS telemetry)
   int rows, cols;
   int unit_begin;          // first column strip of this matrix in the launch
   float scale;
@@ -129,7 +131,51 @@ constexpr int LINE_MAX_MATS = 256;
 struct LineFinalMat {
   const float* part;          // [parts][lines]
   float* inv;                 // [lines]
+  int* nz;                    // optional: count of nonzero lines
   int parts, lines, line_begin;
+};
+
+// sum of squares of the Newton-Schulz output per matrix -> RMS and Eq. (6) scale
+struct OsqFinalParams {
+  const float* part;          // per-tile (x slot) partial sums of O^2
+  long long begin[FIN_MAX_MATS];
+  int count[FIN_MAX_MATS];
+  int out_index[FIN_MAX_MATS];
+  double numel[FIN_MAX_MATS]; // A*B
+  int nmat;
+  float* rms_out;             // optional, indexed by out_index
+  float* scale_out;           // optional: rms_match / RMS (0 for a zero output)
+  float rms_match;
+};
+
+// RMS of a RowNorm direction from its count of nonzero lines: sqrt(nz / (A*B))
+struct NzRmsParams {
+  const int* nz;              // per out_index
+  double numel[FIN_MAX_MATS];
+  int out_index[FIN_MAX_MATS];
+  int nmat;
+  float* rms_out;
+};
+
+// W <- W - eta*(scale_i*O + lambda*W) with O from the workspace (short-side layout)
+constexpr int APPLYWS_MAX_MATS = 256;
+constexpr int APPLYWS_TILE = 64;
+struct ApplyWsMat {
+  void* W;
+  const void* O;              // bf16 (with optional bf16 residual) or fp32, n x ld
+  const void* O_lo;           // bf16 residual or null
+  int n, m, ld;
+  int tall;
+  int tiles_c;                // ceil(m / 64)
+  int tile_begin;
+  int scale_index;
+};
+struct ApplyWsParams {
+  ApplyWsMat mat[APPLYWS_MAX_MATS];
+  int nmat;
+  int total_tiles;
+  const float* scale;         // per scale_index
+  float eta, lam;
 };
 struct LineFinalParams {
   LineFinalMat mat[LINE_MAX_MATS];
@@ -186,7 +232,9 @@ struct NsParams {
   void* dst[NS_MAX_MATS];  // W (apply) or O (output)
   const float* msrc[NS_MAX_MATS];  // fp32 momentum, the exact X0 for the first a*X term
   unsigned char flags[NS_MAX_MATS];  // NS_TALL | NS_MVEC | NS_WVEC
-  int dst_mode;            // 0: O in dst_dtype; 1: apply to W of dst_dtype
+  int dst_mode;            // 0: O in dst_dtype; 1: apply to W of dst_dtype;
+                           // 2: O to X_out (+ residual) in the workspace
+  float* osq_part;         // last UPDATE: partial sums of O^2, [tile][NUM_EPI_WARPS] (or [tile])
   int dst_dtype;           // MUON_DTYPE_*
   float eta, lam, rms_match;
   unsigned int* status;    // device status word
@@ -209,6 +257,7 @@ struct MatPlan {
   size_t line_inv;         // float offset of inverse line norms
   int line_tiles;          // number of partial rows (tiles along the long dim)
   int lines;               // n
+  size_t osq;              // float offset of this matrix's O^2 partials
 };
 
 struct GroupPlan {
@@ -230,6 +279,9 @@ struct Plan {
   size_t inv_norm;         // per matrix 1/||M||
   size_t line_part;
   size_t line_inv;
+  size_t osq_part;         // partial sums of O^2 (telemetry / Eq. (6))
+  size_t scale;            // per matrix Eq. (6) scale
+  size_t nz;               // per matrix nonzero-line counts (int)
   size_t total;
 };
 
@@ -242,6 +294,9 @@ int cols_cluster_size();
 int cols_strip_width(int max_rows, int stage_elem_bytes);
 cudaError_t launch_fro_final(const FroFinalParams& p, cudaStream_t s);
 cudaError_t launch_line_final(const LineFinalParams& p, cudaStream_t s);
+cudaError_t launch_osq_final(const OsqFinalParams& p, cudaStream_t s);
+cudaError_t launch_nz_rms(const NzRmsParams& p, cudaStream_t s);
+cudaError_t launch_apply_ws(int w_dt, int o_dt, const ApplyWsParams& p, cudaStream_t s);
 cudaError_t launch_ns_simt(const NsParams& p, cudaStream_t s);
 cudaError_t launch_ns_tc(const NsParams& p, cudaStream_t s, int num_sms);
 int ns_tc_smem_bytes();
@@ -261,4 +316,7 @@ static_assert(sizeof(FroFinalParams) < 32000, "FroFinalParams too large");
 static_assert(sizeof(LineFinalParams) < 32000, "LineFinalParams too large");
 static_assert(sizeof(NsParams) < 32000, "NsParams too large");
 static_assert(sizeof(ColsParams) < 32000, "ColsParams too large");
+static_assert(sizeof(OsqFinalParams) < 32000, "OsqFinalParams too large");
+static_assert(sizeof(NzRmsParams) < 32000, "NzRmsParams too large");
+static_assert(sizeof(ApplyWsParams) < 32000, "ApplyWsParams too large");
 }  // namespace muon

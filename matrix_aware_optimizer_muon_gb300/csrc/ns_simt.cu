@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(256) ns_simt_kernel(const __grid_constant__ Ns
 
   const float inv = p.inv_norm ? p.inv_norm[gm] : 1.f;
   const float s_apply = p.rms_match * sqrtf((float)m);
+  float osq = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = row0 + ty * 4 + i;
@@ -118,10 +119,16 @@ __global__ void __launch_bounds__(256) ns_simt_kernel(const __grid_constant__ Ns
         const float x = reinterpret_cast<const float*>(G.epi_in)[(size_t)mat * G.stride_nm + (size_t)r * G.ld_m + c];
         const float sc = p.first_iter ? inv : 1.f;
         const float o = sc * (p.a * x + v);
-        if (p.last_iter) ns_last_store(p, gm, n, m, r, c, o, s_apply);
+        osq = fmaf(o, o, osq);
+        if (p.last_iter && p.dst_mode != 2) ns_last_store(p, gm, n, m, r, c, o, s_apply);
         else reinterpret_cast<float*>(G.out)[(size_t)mat * G.stride_nm + (size_t)r * G.ld_m + c] = o;
       }
     }
+  }
+  if (kind == GEMM_UPDATE && p.last_iter && p.osq_part) {   // one partial per 64 x 64 tile
+    __shared__ float red[32];
+    const float t = block_sum(osq, red);
+    if (threadIdx.x == 0) p.osq_part[blockIdx.x] = t;
   }
 }
 

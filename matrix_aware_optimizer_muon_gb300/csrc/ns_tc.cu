@@ -194,8 +194,9 @@ __device__ __forceinline__ void epi_prefetch(const NsParams& p, const NsGroup& G
 }
 
 // Combine and store 32 consecutive columns [c0, c0+32) of row r of one tile.
+template <bool kOsq>
 __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, const Tile& ti, int r, int c0,
-                                           float (&v)[32], const ChunkIn& in) {
+                                           float (&v)[32], const ChunkIn& in, float& osq) {
   const int n = G.n, m = G.m;
   const int gm = G.mat_base + ti.mat;
   if (p.kind == GEMM_UPDATE) {
@@ -234,7 +235,11 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = sc * (p.a * x[j] + v[j]);
-    if (!p.last_iter) {
+    if (kOsq && p.last_iter) {   // sum of squares of the output O (telemetry, Eq. (6))
+#pragma unroll
+      for (int j = 0; j < 32; ++j) osq = (c0 + j < m) ? fmaf(v[j], v[j], osq) : osq;
+    }
+    if (!p.last_iter || p.dst_mode == 2) {
       const size_t off = (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m + c0;
       bf16* Xout = reinterpret_cast<bf16*>(G.out) + off;
       bf16* Lout = G.lo_out ? reinterpret_cast<bf16*>(G.lo_out) + off : nullptr;
@@ -261,6 +266,9 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
 #pragma unroll
         for (int j = 0; j < 32; ++j) w[j] = w[j] - p.eta * (s_apply * v[j] + p.lam * w[j]);
         store_bf16x32(reinterpret_cast<bf16*>(p.dst[gm]) + (size_t)r * m + c0, w);
+      } else if (p.dst_mode == 0 && p.dst_dtype == MUON_DTYPE_BF16 && full && (p.flags[gm] & NS_WVEC)) {
+        // bf16 O output, wide: row r of O, 32 consecutive columns as 16-byte vectors
+        store_bf16x32(reinterpret_cast<bf16*>(p.dst[gm]) + (size_t)r * m + c0, v);
       } else if (in.ok && p.dst_mode == 1 && p.dst_dtype == MUON_DTYPE_BF16 && (p.flags[gm] & NS_TALL)) {
         // tall bf16 W: element (r, c) of the short-side result is W[c][r]
         float w[32];
@@ -319,6 +327,9 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
   }
 }
 
+// kOsq: the last UPDATE also writes per-warp partial sums of O^2 (only launches
+// that need them pay for them).
+template <bool kOsq>
 __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_constant__ NsParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -454,6 +465,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
       const int r = ti.tm * BM + row_in_tile;
       const int cbase = ti.tn * BN + half * (EPI_CHUNKS * 32);
       ChunkIn in[2];
+      float osq = 0.f;
       epi_prefetch(p, G, ti, r, cbase, in[0]);   // does not depend on this tile's accumulator
       int ok = 1;
       if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, p, true) ? 1 : 0;
@@ -466,7 +478,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
         float v[32];
         ptx::tmem_ld_32x32b_x32(tbase + k * 32, v);
         if (k + 1 < EPI_CHUNKS) epi_prefetch(p, G, ti, r, cbase + (k + 1) * 32, in[(k + 1) & 1]);
-        epi_finish(p, G, ti, r, cbase + k * 32, v, in[k & 1]);
+        epi_finish<kOsq>(p, G, ti, r, cbase + k * 32, v, in[k & 1], osq);
+      }
+      if (kOsq && p.last_iter) {   // one fixed slot per (tile, epilogue warp)
+        osq = warp_sum(osq);
+        if (lane == 0) p.osq_part[(size_t)t * NUM_EPI_WARPS + (warp - 2)] = osq;
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -491,12 +507,15 @@ cudaError_t launch_ns_tc(const NsParams& p, cudaStream_t s, int num_sms) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(tc::ns_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    e = cudaFuncSetAttribute(tc::ns_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(tc::ns_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
-  tc::ns_tc_kernel<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, s>>>(p);
+  if (p.osq_part && p.last_iter) tc::ns_tc_kernel<true><<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, s>>>(p);
+  else tc::ns_tc_kernel<false><<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, s>>>(p);
   return cudaGetLastError();
 }
 

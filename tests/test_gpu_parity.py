@@ -440,3 +440,79 @@ def test_cuda_graph_capture_matches_eager():
     assert mm.muon_check_status(ws) == mm.MUON_OK
     for a, b in zip(We + Me, Wg + Mg):
         assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# Eq. (6) Update Norm and update-RMS telemetry
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt,mode", [("bf16", "bf16"), ("f32", "f32")])
+def test_update_norm_refresh_step_parity(dt, mode):
+    shapes = [(256, 1024), (1024, 256), (300, 1000), (1000, 300), (129, 129), (33, 100)]
+    W0, Gs = inputs(shapes, dt, dt, 1)
+    M0 = [mixed_momentum(s, 3, seed=20 + i) for i, s in enumerate(shapes)]
+    W = [to_dev(w, dt) for w in W0]
+    M = [to_dev(m, "f32") for m in M0]
+    G = [to_dev(g, dt) for g in Gs[0]]
+    ws = mm.alloc_workspace(shapes, mode)
+    rms = torch.full((len(shapes),), -1.0, device=dev())
+    br = mm.muon_periodic_step(W, G, M, 3, ws, K=3, ns5_mode=mode, scale_mode="update_norm", update_rms=rms)
+    assert br == mm.MUON_BRANCH_NS5
+    torch.cuda.synchronize()
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+    tol = TOL_NS5_BF16 if mode == "bf16" else TOL_NS5_F32
+    for i, (a, b) in enumerate(shapes):
+        refW, refM, refresh, refrms = muon_ref.periodic_step(W0[i], M0[i], Gs[0][i], 3, 3, 0.15, 0.95, 0.02, 0.01,
+                                                             scale_mode="update_norm", telemetry=True)
+        assert refresh
+        assert_f32_close(to_np(M[i]), refM, what=f"M {shapes[i]}")
+        ulp = 2.0 ** -23 if dt == "f32" else 2.0 ** -7
+        dW = refW - W0[i]
+        assert np.linalg.norm(to_np(W[i]) - refW) <= tol * np.linalg.norm(dW) + np.linalg.norm(np.abs(refW)) * ulp, \
+            shapes[i]
+        assert abs(float(rms[i]) - refrms) <= tol * refrms, (shapes[i], float(rms[i]), refrms)
+        # Eq. (6): the applied direction has RMS 0.2 exactly -> |dW + eta*lam*W| has RMS eta*0.2
+        got_dir = (to_np(W[i]) - W0[i] * (1 - 0.02 * 0.01)) / -0.02
+        assert abs(muon_ref.rms(got_dir) - 0.2) <= tol * 0.2 + np.linalg.norm(np.abs(refW)) * ulp / 0.02 / math.sqrt(a * b)
+
+
+@pytest.mark.parametrize("path", ["cluster", "two_pass"])
+def test_update_rms_telemetry(path):
+    shapes = [(256, 1024), (1000, 300), (4608, 1536), (1536, 6144), (300, 36), (13, 7), (0, 5), (40000, 8)]
+    W0, Gs = inputs(shapes, "bf16", "bf16", 2)
+    M0 = rand_M(shapes, seed=21, zero_line=True)
+    for i, (a, b) in enumerate(shapes):   # keep the zero line zero through the momentum step
+        if a > 2 and b > 2:
+            if a <= b:
+                Gs[1][i][1, :] = 0.0
+            else:
+                Gs[1][i][:, 1] = 0.0
+    W = [to_dev(w, "bf16") for w in W0]
+    M = [to_dev(m, "f32") for m in M0]
+    ws = mm.alloc_workspace(shapes)
+    rms = torch.full((len(shapes),), -1.0, device=dev())
+    mm.muon_debug_set(mm.MUON_DEBUG_NO_CLUSTER if path == "two_pass" else 0, 0)
+    try:
+        # RowNorm step (scale_mode update_norm equals Eq. (7) when no line is zero; here some are)
+        G = [to_dev(g, "bf16") for g in Gs[1]]
+        mm.muon_periodic_step(W, G, M, 1, ws, update_rms=rms)
+    finally:
+        mm.muon_debug_set(0, 0)
+    torch.cuda.synchronize()
+    for i, s in enumerate(shapes):
+        if 0 in s:
+            assert float(rms[i]) == 0.0
+            continue
+        refW, refM, _, refrms = muon_ref.periodic_step(W0[i], M0[i], Gs[1][i], 1, telemetry=True, w_dtype="bf16")
+        assert abs(float(rms[i]) - refrms) <= 1e-6 * refrms, (s, float(rms[i]), refrms)
+    # refresh step telemetry against the oracle's RMS(O)
+    rms.fill_(-1.0)
+    G = [to_dev(g, "bf16") for g in Gs[0]]
+    M2 = [to_dev(m, "f32") for m in M0]
+    W2 = [to_dev(w, "bf16") for w in W0]
+    mm.muon_periodic_step(W2, G, M2, 0, ws, update_rms=rms)
+    torch.cuda.synchronize()
+    for i, s in enumerate(shapes):
+        if 0 in s:
+            continue
+        *_, refrms = muon_ref.periodic_step(W0[i], M0[i], Gs[0][i], 0, telemetry=True)
+        assert abs(float(rms[i]) - refrms) <= TOL_NS5_BF16 * refrms, (s, float(rms[i]), refrms)
