@@ -245,3 +245,37 @@ def polar_factor(M: np.ndarray) -> np.ndarray:
 def rms(X: np.ndarray) -> float:
     X = np.asarray(X, dtype=np.float64)
     return float(np.sqrt(np.mean(X * X))) if X.size else 0.0
+
+
+# ---------------------------------------------------------------------------
+# AdamW for the parameters Muon does not take
+# ---------------------------------------------------------------------------
+ADAMW_BETA1 = 0.9
+ADAMW_BETA2 = 0.999
+ADAMW_EPS = 1e-8
+ADAMW_AUX_LR = 1e-4   # Scaling Muon for Diffusion Transformers (summary page): auxiliary AdamW group
+
+
+def adamw_step(p: np.ndarray, g: np.ndarray, m: np.ndarray, v: np.ndarray, t: int, lr: float,
+               beta1: float = ADAMW_BETA1, beta2: float = ADAMW_BETA2, eps: float = ADAMW_EPS,
+               weight_decay: float = 0.0):
+    """One AdamW step (Adam moments with bias correction, decoupled weight decay) on a
+    parameter that Muon does not update.
+
+    Scaling Muon for Diffusion Transformers (summary page, experimental setup): bias,
+    normalisation and out-of-block parameters keep AdamW; an auxiliary AdamW group uses
+    LR 1e-4.  Muon is Scalable for LLM Training (notes, section 2.2, "Matching update RMS
+    of AdamW"): Muon and AdamW share the learning rate and weight decay.  The pages give
+    no betas or epsilon; the reading here is the usual (0.9, 0.999, 1e-8).  t counts
+    steps from 1.  Returns (p, m, v).
+    """
+    if t < 1:
+        raise ValueError("t counts from 1")
+    p = np.asarray(p, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    m = beta1 * np.asarray(m, dtype=np.float64) + (1.0 - beta1) * g
+    v = beta2 * np.asarray(v, dtype=np.float64) + (1.0 - beta2) * g * g
+    m_hat = m / (1.0 - beta1 ** t)
+    v_hat = v / (1.0 - beta2 ** t)
+    p = p - lr * (m_hat / (np.sqrt(v_hat) + eps) + weight_decay * p)
+    return p, m, v

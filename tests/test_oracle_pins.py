@@ -334,11 +334,46 @@ def check_update_rms(o):
         assert abs(out[3] - math.sqrt(sum(Uo[i][j] ** 2 for i in range(A) for j in range(B)) / (A * B))) < 1e-12
 
 
+def check_adamw(o):
+    """AdamW against torch.optim.AdamW (a library routine, float64), a closed form of
+    the first step, and a scalar brute-force loop."""
+    rng = np.random.default_rng(15)
+    p0 = rng.standard_normal(37)
+    gs = [rng.standard_normal(37) * 10.0 ** rng.uniform(-4, 0) for _ in range(6)]
+    lr, wd = 3e-3, 0.01
+    torch = pytest.importorskip("torch")
+    tp = torch.tensor(p0.copy(), dtype=torch.float64, requires_grad=True)
+    opt = torch.optim.AdamW([tp], lr=lr, betas=(0.9, 0.999), eps=1e-8, weight_decay=wd)
+    p, m, v = p0.copy(), np.zeros(37), np.zeros(37)
+    for t, g in enumerate(gs, start=1):
+        tp.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+        p, m, v = o.adamw_step(p, g, m, v, t, lr, weight_decay=wd)
+        assert np.max(np.abs(p - tp.detach().numpy())) < 1e-12, t
+    # first step: m_hat = g, v_hat = g^2, so the step is lr*(g/(|g|+eps) + wd*p)
+    g = rng.standard_normal(9)
+    q = rng.standard_normal(9)
+    p1, m1, v1 = o.adamw_step(q, g, np.zeros(9), np.zeros(9), 1, 0.5, weight_decay=0.1)
+    assert np.max(np.abs(p1 - (q - 0.5 * (g / (np.abs(g) + 1e-8) + 0.1 * q)))) < 1e-12
+    assert np.max(np.abs(m1 - 0.1 * g)) < 1e-15 and np.max(np.abs(v1 - 0.001 * g * g)) < 1e-15
+    # scalar brute force, third step with nonzero state
+    pp, mm_, vv = 0.3, 0.02, 1e-4
+    gg = -0.7
+    b1, b2 = 0.9, 0.999
+    m2 = b1 * mm_ + (1 - b1) * gg
+    v2 = b2 * vv + (1 - b2) * gg * gg
+    want = pp - 0.01 * ((m2 / (1 - b1 ** 3)) / (math.sqrt(v2 / (1 - b2 ** 3)) + 1e-8) + 0.05 * pp)
+    got = o.adamw_step(np.array([pp]), np.array([gg]), np.array([mm_]), np.array([vv]), 3, 0.01,
+                       weight_decay=0.05)[0][0]
+    assert abs(got - want) < 1e-15
+    assert o.ADAMW_AUX_LR == GOLDEN["adamw_aux_lr"]["value"]
+
+
 ALL_CHECKS = [check_constants, check_ns5_closed_form, check_ns5_diagonal, check_ns5_orthogonal_input,
               check_ns5_polar_and_band, check_ns5_short_side, check_ns5_scale_and_zero,
               check_rownorm_bruteforce, check_rownorm_invariants, check_lemma1, check_momentum,
               check_apply, check_scale, check_schedule, check_step, check_bf16_rounding, check_update_norm,
-              check_update_rms]
+              check_update_rms, check_adamw]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
@@ -383,6 +418,11 @@ MUTATIONS = [
     ("q = np.rint(np.ldexp(frac, 8))", "q = np.floor(np.ldexp(frac, 8) + 0.5)"),
     ("U = muon_direction(M, refresh)", "U = muon_direction(M_prev, refresh)"),
     ("    s = RMS_MATCH / r\n", "    s = RMS_MATCH * r\n"),
+    ("    v = beta2 * np.asarray(v, dtype=np.float64) + (1.0 - beta2) * g * g",
+     "    v = beta2 * np.asarray(v, dtype=np.float64) + (1.0 - beta2) * g"),
+    ("    m_hat = m / (1.0 - beta1 ** t)", "    m_hat = m"),
+    ("    p = p - lr * (m_hat / (np.sqrt(v_hat) + eps) + weight_decay * p)",
+     "    p = p - lr * (m_hat / (np.sqrt(v_hat) + eps)) - weight_decay * p"),
     ("nz = int(np.count_nonzero(np.sqrt(np.sum(U * U, axis=line_axis)) > 0.0))", "nz = min(A, B)"),
     ("        r = rms(U)\n", "        r = math.sqrt(float(np.mean(np.abs(U))))\n"),
 ]
