@@ -190,6 +190,30 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
                           const muon_step_options* opts, void* ws, size_t ws_bytes,
                           muon_stream_t stream, int* branch_out);
 
+/* A parameter that Muon does not update (bias, normalisation weight, out-of-block
+ * parameter), with its AdamW state. */
+typedef struct muon_adamw_param {
+  void* P;          /* device, numel elements of p_dtype; updated in place            */
+  const void* G;    /* device, numel elements of g_dtype                             */
+  float* m;         /* device, numel fp32 first moment (starts at 0)                 */
+  float* v;         /* device, numel fp32 second moment (starts at 0)                */
+  int64_t numel;
+  int32_t p_dtype;  /* MUON_DTYPE_F32 or MUON_DTYPE_BF16                             */
+  int32_t g_dtype;  /* MUON_DTYPE_F32 or MUON_DTYPE_BF16                             */
+} muon_adamw_param;
+
+/* AdamW on the parameters beside the Muon matrices ("Scaling Muon for Diffusion
+ * Transformers", summary page: bias, normalisation and out-of-block parameters
+ * keep AdamW, an auxiliary group at LR 1e-4; "Muon is Scalable" notes, section
+ * 2.2: the two optimizers share learning rate and weight decay):
+ *   m <- b1*m + (1-b1)*g;  v <- b2*v + (1-b2)*g^2;
+ *   p <- p - lr*( (m/(1-b1^t)) / (sqrt(v/(1-b2^t)) + eps) + weight_decay*p ),
+ * fp32 arithmetic, one rounding to p_dtype (beta1 and beta2 are double so that 1-beta
+ * is exact enough: 0.999 in fp32 would put 1.3e-5 into 1-beta2).  t counts steps from 1.  One launch
+ * covers the whole list (host array); every entry uses the same dtype pair. */
+int muon_adamw_step(const muon_adamw_param* params, int n, int64_t t, float lr, double beta1,
+                    double beta2, float eps, float weight_decay, muon_stream_t stream);
+
 /* Synchronises `stream`, reads and clears the device status word in `ws`, and
  * returns MUON_OK or the recorded error (MUON_ERR_TIMEOUT). */
 int muon_check_status(void* ws, size_t ws_bytes, muon_stream_t stream);

@@ -9,7 +9,7 @@ from ._lib import (MUON_BRANCH_NS5, MUON_BRANCH_ROWNORM, MUON_DEBUG_NO_CLUSTER, 
                    MuonMatrix, alloc_workspace, load_library, make_matrices, muon_apply, muon_check_status,
                    muon_debug_set, muon_fro_norm, muon_fro_norm_noalloc, muon_momentum, muon_ns5_batched, muon_periodic_step,
                    muon_rownorm, muon_workspace_init, muon_workspace_size, status_str,
-                   muon_profile_events, muon_launch_count)
+                   muon_profile_events, muon_launch_count, muon_adamw_step)
 from .optim import PeriodicMuon
 
 __all__ = [n for n in dir() if not n.startswith("_")]

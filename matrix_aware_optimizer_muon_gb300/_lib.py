@@ -51,6 +51,11 @@ class MuonStepOptions(ctypes.Structure):
     _fields_ = [("scale_mode", ctypes.c_int), ("update_rms", ctypes.c_void_p)]
 
 
+class MuonAdamwParam(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_void_p), ("G", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("numel", ctypes.c_int64), ("p_dtype", ctypes.c_int32), ("g_dtype", ctypes.c_int32)]
+
+
 class MuonMatrix(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("G", ctypes.c_void_p), ("M", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
@@ -90,6 +95,8 @@ def load_library(path: Optional[str] = None):
         "muon_abi_version": (i32, []),
         "muon_debug_set": (i32, [i32, i32]),
         "muon_profile_events": (i32, [ptrs, i32]),
+        "muon_adamw_step": (i32, [ctypes.POINTER(MuonAdamwParam), i32, i64, f32, ctypes.c_double, ctypes.c_double,
+                                  f32, f32, vp]),
         "muon_launch_count": (i32, []),
     }
     for name, (res, args) in sig.items():
@@ -283,3 +290,20 @@ def muon_profile_events(events: Sequence) -> None:
 
 def muon_launch_count() -> int:
     return int(load_library().muon_launch_count())
+
+
+def muon_adamw_step(P: Sequence[torch.Tensor], G: Sequence[torch.Tensor], m: Sequence[torch.Tensor],
+                    v: Sequence[torch.Tensor], t: int, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+                    eps: float = 1e-8, weight_decay: float = 0.0, stream=None):
+    """AdamW on parameters Muon does not take (any shape; m, v fp32 of the same size)."""
+    n = len(P)
+    arr = (MuonAdamwParam * max(n, 1))()
+    for i in range(n):
+        if not (P[i].numel() == G[i].numel() == m[i].numel() == v[i].numel()):
+            raise ValueError("P, G, m, v must have the same number of elements")
+        if m[i].dtype != torch.float32 or v[i].dtype != torch.float32:
+            raise ValueError("AdamW moments are fp32")
+        arr[i] = MuonAdamwParam(_ptr(P[i]), _ptr(G[i]), _ptr(m[i]), _ptr(v[i]), int(P[i].numel()),
+                                _dt(P[i]), _dt(G[i]))
+    _check("muon_adamw_step", load_library().muon_adamw_step(arr, n, int(t), lr, beta1, beta2, eps,
+                                                             weight_decay, _stream(stream)))

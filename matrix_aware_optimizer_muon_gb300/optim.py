@@ -16,8 +16,16 @@ class PeriodicMuon:
     """
 
     def __init__(self, params: Sequence[torch.Tensor], K: int = 3, gamma: float = 0.15, mu: float = 0.95,
-                 eta: float = 0.02, lam: float = 0.01, ns5_mode: str = "bf16"):
+                 eta: float = 0.02, lam: float = 0.01, ns5_mode: str = "bf16",
+                 aux_params: Sequence[torch.Tensor] = (), aux_lr: float = 1e-4, betas=(0.9, 0.999),
+                 eps: float = 1e-8):
+        """aux_params: parameters Muon does not take (biases, norms, out-of-block weights);
+        they are updated by AdamW with learning rate aux_lr and the shared weight decay lam."""
         self.params: List[torch.Tensor] = list(params)
+        self.aux = list(aux_params)
+        self.aux_lr, self.betas, self.eps = aux_lr, betas, eps
+        self.aux_m = [torch.zeros(p.numel(), dtype=torch.float32, device=p.device) for p in self.aux]
+        self.aux_v = [torch.zeros(p.numel(), dtype=torch.float32, device=p.device) for p in self.aux]
         if not self.params:
             raise ValueError("no parameters")
         self.K, self.gamma, self.mu, self.eta, self.lam, self.ns5_mode = K, gamma, mu, eta, lam, ns5_mode
@@ -26,10 +34,16 @@ class PeriodicMuon:
         self.ws = _lib.alloc_workspace([tuple(p.shape) for p in self.params], ns5_mode, device=dev)
         self.step_count = 0
 
-    def step(self, grads: Sequence[torch.Tensor], stream=None) -> int:
+    def step(self, grads: Sequence[torch.Tensor], aux_grads: Sequence[torch.Tensor] = (), stream=None) -> int:
         br = _lib.muon_periodic_step(self.params, grads, self.M, self.step_count, self.ws, K=self.K,
                                      gamma=self.gamma, mu=self.mu, eta=self.eta, lam=self.lam,
                                      ns5_mode=self.ns5_mode, stream=stream)
+        if self.aux:
+            if len(aux_grads) != len(self.aux):
+                raise ValueError("one gradient per auxiliary parameter")
+            _lib.muon_adamw_step([p.view(-1) for p in self.aux], [g.reshape(-1) for g in aux_grads], self.aux_m,
+                                 self.aux_v, self.step_count + 1, self.aux_lr, self.betas[0], self.betas[1],
+                                 self.eps, self.lam, stream=stream)
         self.step_count += 1
         return br
 
@@ -38,6 +52,7 @@ class PeriodicMuon:
 
     def state_dict(self) -> Dict:
         return {"step": self.step_count, "M": [m.detach().clone() for m in self.M],
+                "aux_m": [m.detach().clone() for m in self.aux_m], "aux_v": [v.detach().clone() for v in self.aux_v],
                 "hyper": dict(K=self.K, gamma=self.gamma, mu=self.mu, eta=self.eta, lam=self.lam,
                               ns5_mode=self.ns5_mode)}
 
@@ -47,5 +62,7 @@ class PeriodicMuon:
         for dst, src in zip(self.M, sd["M"]):
             if tuple(dst.shape) != tuple(src.shape):
                 raise ValueError("state shape mismatch")
+            dst.copy_(src)
+        for dst, src in zip(self.aux_m + self.aux_v, sd.get("aux_m", []) + sd.get("aux_v", [])):
             dst.copy_(src)
         self.step_count = int(sd["step"])

@@ -516,3 +516,40 @@ def test_update_rms_telemetry(path):
             continue
         *_, refrms = muon_ref.periodic_step(W0[i], M0[i], Gs[0][i], 0, telemetry=True)
         assert abs(float(rms[i]) - refrms) <= TOL_NS5_BF16 * refrms, (s, float(rms[i]), refrms)
+
+
+# ---------------------------------------------------------------------------
+# AdamW beside Muon (biases, norms, out-of-block parameters)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("pdt,gdt", [("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16")])
+def test_adamw_parity(pdt, gdt):
+    sizes = [1, 7, 1536, 4097, 9216, 100003]
+    rng = np.random.default_rng(30)
+    P0 = [quantize_np((rng.standard_normal(k) * 0.02).astype(np.float32), pdt) for k in sizes]
+    P = [to_dev(p, pdt) for p in P0]
+    m = [torch.zeros(k, device=dev()) for k in sizes]
+    v = [torch.zeros(k, device=dev()) for k in sizes]
+    refP = [p.astype(np.float64) for p in P0]
+    refm = [np.zeros(k) for k in sizes]
+    refv = [np.zeros(k) for k in sizes]
+    lr, wd = 1e-4, 0.01
+    for t in range(1, 5):
+        Gn = [quantize_np((rng.standard_normal(k) * 10.0 ** rng.uniform(-4, -1)).astype(np.float32), gdt) for k in sizes]
+        # teacher forcing on p: the GPU starts each step from the oracle's parameter
+        for i in range(len(sizes)):
+            P[i].copy_(to_dev(refP[i].astype(np.float32), pdt))
+        mm.muon_adamw_step(P, [to_dev(g, gdt) for g in Gn], m, v, t, lr, weight_decay=wd)
+        torch.cuda.synchronize()
+        for i, k in enumerate(sizes):
+            prev = refP[i]
+            refP[i], refm[i], refv[i] = muon_ref.adamw_step(refP[i], Gn[i], refm[i], refv[i], t, lr, weight_decay=wd)
+            assert_f32_close(to_np(m[i]), refm[i], what=f"m {k} t={t}")
+            assert_f32_close(to_np(v[i]), refv[i], what=f"v {k} t={t}")
+            step = prev - refP[i]
+            terms = np.abs(prev) + np.abs(step)
+            if pdt == "f32":
+                d = np.abs(to_np(P[i]) - refP[i])
+                assert np.all(d <= 1e-5 * terms + 1e-30), (k, t, float(np.max(d / (terms + 1e-30))))
+            else:
+                assert_bf16_close(to_np(P[i]), refP[i], terms, what=f"p {k} t={t}")
+            refP[i] = muon_ref.round_to_storage(refP[i], pdt)
