@@ -376,27 +376,64 @@ def run_ours(args, torch):
         "wall_s": round(wall, 3),
     }
 
-    # end-to-end through the public API with host buffers (pinned), copies inside the timed region
+    # End to end through the public API with host buffers (pinned): every optimizer step
+    # uploads its gradients and downloads its updated weights inside the timed region.
+    # Copies are pipelined with compute the way a training loop would run them: G is
+    # double-buffered on the device (the upload for step t+1 runs during step t), and
+    # W is staged on the device after each step so that its download overlaps the
+    # next step.
     if not args.no_e2e:
         G_host = torch.empty(tot, dtype=gdt, pin_memory=True)
         W_host = torch.empty(tot, dtype=wdt, pin_memory=True)
         G_host.copy_(G_flat)
+        G2_flat = torch.empty_like(G_flat)
+        W_stage = torch.empty_like(W_flat)
+        G_bufs = [G_flat, G2_flat]
+        G_views = [[gb[o:o + a * b].view(a, b) for o, (a, b) in zip(offs, shapes)] for gb in G_bufs]
+        comp = torch.cuda.current_stream()
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
         torch.cuda.synchronize()
+        n_e2e = max(1, min(args.steps, 5)) * wl.K
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
+        staged = torch.cuda.Event()
+        downloaded = torch.cuda.Event()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_e2e = max(1, min(args.steps, 5))
         barrier(dist)
-        e0.record()
-        for _ in range(n_e2e):
-            for _ in range(wl.K):
-                G_flat.copy_(G_host, non_blocking=True)
-                opt_step(step_counter[0])
-                step_counter[0] += 1
-                W_host.copy_(W_flat, non_blocking=True)
-        e1.record()
+        e0.record(comp)
+        with torch.cuda.stream(up):
+            up.wait_event(e0)
+            G_bufs[0].copy_(G_host, non_blocking=True)
+            uploaded[0].record(up)
+        downloaded.record(comp)
+        for i in range(n_e2e):
+            cur = i & 1
+            if i + 1 < n_e2e:                     # upload the next step's gradients now
+                with torch.cuda.stream(up):
+                    if i >= 1:
+                        up.wait_event(consumed[1 - cur])
+                    G_bufs[1 - cur].copy_(G_host, non_blocking=True)
+                    uploaded[1 - cur].record(up)
+            comp.wait_event(uploaded[cur])
+            mm.muon_periodic_step(W, G_views[cur], M, step_counter[0], ws, K=wl.K, gamma=wl.gamma, mu=wl.mu,
+                                  eta=wl.eta, lam=wl.lam, ns5_mode=mode)
+            step_counter[0] += 1
+            consumed[cur].record(comp)
+            comp.wait_event(downloaded)           # the previous download has left the stage
+            W_stage.copy_(W_flat, non_blocking=True)
+            staged.record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(staged)
+                W_host.copy_(W_stage, non_blocking=True)
+                downloaded.record(down)
+        comp.wait_event(downloaded)
+        e1.record(comp)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / (n_e2e * wl.K), device)
+        e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / n_e2e, device)
         line["e2e"] = {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": tot * gb,
-                       "d2h_bytes_per_step": tot * wb, "periods": n_e2e}
+                       "d2h_bytes_per_step": tot * wb, "steps": n_e2e,
+                       "note": "G uploaded and W downloaded every step from/to pinned host memory, "
+                               "pipelined with compute (double-buffered G, W staged on the device)"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, detail = oracle_sample(wl)

@@ -553,3 +553,34 @@ def test_adamw_parity(pdt, gdt):
             else:
                 assert_bf16_close(to_np(P[i]), refP[i], terms, what=f"p {k} t={t}")
             refP[i] = muon_ref.round_to_storage(refP[i], pdt)
+
+
+def test_periodic_muon_wrapper_matches_direct_calls():
+    """The stateful wrapper (momentum buffers, workspace, step counter, auxiliary AdamW)
+    gives the same bits as calling the entry points directly."""
+    shapes = [(300, 1000), (1000, 300)]
+    W0, Gs = inputs(shapes, "bf16", "bf16", 4)
+    rng = np.random.default_rng(40)
+    B0 = [(rng.standard_normal(a) * 0.01).astype(np.float32) for a, _ in shapes]
+    Bg = [[(rng.standard_normal(a) * 1e-3).astype(np.float32) for a, _ in shapes] for _ in range(4)]
+    Wa = [to_dev(w, "bf16") for w in W0]
+    Ba = [to_dev(b, "f32") for b in B0]
+    opt = mm.PeriodicMuon(Wa, aux_params=Ba, aux_lr=1e-4)
+    Wb = [to_dev(w, "bf16") for w in W0]
+    Bb = [to_dev(b, "f32") for b in B0]
+    Mb = [torch.zeros(s, device=dev()) for s in shapes]
+    mb = [torch.zeros(a, device=dev()) for a, _ in shapes]
+    vb = [torch.zeros(a, device=dev()) for a, _ in shapes]
+    ws = mm.alloc_workspace(shapes)
+    for t in range(4):
+        G = [to_dev(g, "bf16") for g in Gs[t]]
+        bg = [to_dev(g, "f32") for g in Bg[t]]
+        assert opt.step(G, bg) == (1 if t % 3 == 0 else 0)
+        mm.muon_periodic_step(Wb, G, Mb, t, ws)
+        mm.muon_adamw_step(Bb, bg, mb, vb, t + 1, 1e-4, weight_decay=0.01)
+    torch.cuda.synchronize()
+    assert opt.check() == mm.MUON_OK
+    for a, b in zip(Wa + Ba + opt.M, Wb + Bb + Mb):
+        assert torch.equal(a, b)
+    sd = opt.state_dict()
+    assert sd["step"] == 4 and len(sd["aux_m"]) == 2
