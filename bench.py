@@ -34,7 +34,7 @@ L2_BYTES = 129e6
 # set (the same shape mix, 1/8 of the matrices) scaled by 8; see
 # profiles/ns_tc_kernel_traffic_mmdit-1.3b.md.  Valid only for the kernel sources
 # it was measured on (hash below); otherwise the roofline reports null.
-NS5_TRAFFIC = {"mmdit-1.3b": {"bytes_per_launch": 4.70e9, "sources": "91bd98069111257b"}}
+NS5_TRAFFIC = {"mmdit-1.3b": {"bytes_per_launch": 4.70e9, "sources": "a2a9fb43c12720b7"}}
 NS5_SOURCES = ["ns_tc.cu", "ns_common.cuh", "ptx.cuh", "common.cuh", "internal.h", "api.cu"]
 
 
@@ -430,10 +430,28 @@ def run_ours(args, torch):
         e1.record(comp)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / n_e2e, device)
+        # The same copies with no compute between them: the floor the host link sets.
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(comp)
+        for s_, dst, src in ((up, G_bufs, G_host), (down, None, W_stage)):
+            with torch.cuda.stream(s_):
+                s_.wait_event(l0)
+                for i in range(n_e2e):
+                    if dst is None:
+                        W_host.copy_(src, non_blocking=True)
+                    else:
+                        dst[i & 1].copy_(src, non_blocking=True)
+            comp.wait_stream(s_)
+        l1.record(comp)
+        torch.cuda.synchronize()
+        link_ms = max_over_ranks(torch, dist, l0.elapsed_time(l1) / n_e2e, device)
         line["e2e"] = {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": tot * gb,
                        "d2h_bytes_per_step": tot * wb, "steps": n_e2e,
+                       "copies_alone_ms": round(link_ms, 4),
+                       "copies_alone_gbs": round((tot * gb + tot * wb) / link_ms / 1e6, 1),
                        "note": "G uploaded and W downloaded every step from/to pinned host memory, "
-                               "pipelined with compute (double-buffered G, W staged on the device)"}
+                               "pipelined with compute (double-buffered G, W staged on the device); "
+                               "copies_alone_ms: the same copies with no compute"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, detail = oracle_sample(wl)

@@ -240,13 +240,21 @@ int muon_abi_version(void);
 /* Test hooks (process-wide, not for production use).
  * timeout_ms: limit of every device-side wait (default 4000 ms; 0 restores it).
  * flags: MUON_DEBUG_STALL_PRODUCER makes the tensor-core GEMM's load warp issue
- * nothing, so that its consumers' bounded waits expire and report
- * MUON_ERR_TIMEOUT through muon_check_status (no fault, no hang).
- * MUON_DEBUG_NO_CLUSTER sends tall matrices of RowNorm steps through the
- * two-pass kernels instead of the single-pass cluster kernel (to test both).
+ * nothing, and the tall-matrix RowNorm kernel publish no column norms, so that
+ * their consumers' bounded waits expire and report MUON_ERR_TIMEOUT through
+ * muon_check_status (no fault, no hang).
+ * Tall matrices of RowNorm steps normally take two row-contiguous passes whose
+ * second pass re-reads the new momentum from L2.  MUON_DEBUG_NO_CLUSTER sends
+ * them through the plain two-pass kernels instead, MUON_DEBUG_TALL_CLUSTER
+ * through the single-pass thread-block-cluster kernel (to test every path).
  * MUON_DEBUG_NO_OVERLAP runs the wide-row and tall-column kernels of a RowNorm
  * step one after the other on the caller's stream instead of side by side. */
-enum { MUON_DEBUG_STALL_PRODUCER = 1, MUON_DEBUG_NO_CLUSTER = 2, MUON_DEBUG_NO_OVERLAP = 4 };
+enum {
+  MUON_DEBUG_STALL_PRODUCER = 1,
+  MUON_DEBUG_NO_CLUSTER = 2,
+  MUON_DEBUG_NO_OVERLAP = 4,
+  MUON_DEBUG_TALL_CLUSTER = 8
+};
 int muon_debug_set(int flags, int timeout_ms);
 
 #ifdef __cplusplus

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmuon_gb300.so")
-SOURCES = ["api.cu", "ew.cu", "cols.cu", "ns_tc.cu", "ns_simt.cu", "noalloc.cu", "adamw.cu"]
+SOURCES = ["api.cu", "ew.cu", "cols.cu", "ns_tc.cu", "ns_simt.cu", "noalloc.cu", "adamw.cu", "tall.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -47,6 +47,21 @@ __device__ __forceinline__ float adamw_one(float& p, float g, float& m, float& v
   return p;
 }
 
+// Elements i .. i+3 (those below numel) one at a time.
+template <typename PT, typename GT>
+__device__ __forceinline__ void adamw_tail(PT* P, const GT* G, const AdamwEntry& e, long long i, const AdamwParams& q) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (i + j < e.numel) {
+      float p = ld1(P + i + j), m = e.m[i + j], v = e.v[i + j];
+      adamw_one(p, ld1(G + i + j), m, v, q);
+      st1(P + i + j, p);
+      e.m[i + j] = m;
+      e.v[i + j] = v;
+    }
+  }
+}
+
 template <typename PT, typename GT>
 __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamwParams q) {
   int lo = 0, hi = q.n - 1;
@@ -59,32 +74,43 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
   const long long e0 = (long long)(b - e.block_begin) * ADAMW_CHUNK;
   PT* P = reinterpret_cast<PT*>(e.P);
   const GT* G = reinterpret_cast<const GT*>(e.G);
+  constexpr int KC = ADAMW_CHUNK / (256 * 4);
+  if (e.vec) {
+    // all loads of the block first, then the updates: one DRAM round trip per thread
+    typename Raw4<PT>::type pr[KC];
+    typename Raw4<GT>::type gr[KC];
+    float4 mr[KC], vr[KC];
 #pragma unroll
-  for (int k = 0; k < ADAMW_CHUNK / (256 * 4); ++k) {
-    const long long i = e0 + (long long)(k * 256 + threadIdx.x) * 4;
-    if (e.vec && i + 4 <= e.numel) {
-      float p[4], g[4], m[4], v[4];
-      ld4(P + i, p);
-      ld4_stream(G + i, g);
-      ld4(e.m + i, m);
-      ld4(e.v + i, v);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) adamw_one(p[j], g[j], m[j], v[j], q);
-      st4(P + i, p);
-      st4(e.m + i, m);
-      st4(e.v + i, v);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (i + j < e.numel) {
-          float p = ld1(P + i + j), m = e.m[i + j], v = e.v[i + j];
-          adamw_one(p, ld1(G + i + j), m, v, q);
-          st1(P + i + j, p);
-          e.m[i + j] = m;
-          e.v[i + j] = v;
-        }
+    for (int k = 0; k < KC; ++k) {
+      const long long i = e0 + (long long)(k * 256 + threadIdx.x) * 4;
+      if (i + 4 <= e.numel) {
+        pr[k] = ldraw(P + i);
+        gr[k] = ldraw_stream(G + i);
+        mr[k] = ldraw(e.m + i);
+        vr[k] = ldraw(e.v + i);
       }
     }
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+      const long long i = e0 + (long long)(k * 256 + threadIdx.x) * 4;
+      if (i + 4 <= e.numel) {
+        float p[4], g[4], m[4], v[4];
+        cvt4(pr[k], p);
+        cvt4(gr[k], g);
+        cvt4(mr[k], m);
+        cvt4(vr[k], v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) adamw_one(p[j], g[j], m[j], v[j], q);
+        st4(P + i, p);
+        st4(e.m + i, m);
+        st4(e.v + i, v);
+      } else {
+        adamw_tail(P, G, e, i, q);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < KC; ++k) adamw_tail(P, G, e, e0 + (long long)(k * 256 + threadIdx.x) * 4, q);
   }
 }
 

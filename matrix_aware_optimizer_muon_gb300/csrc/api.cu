@@ -108,6 +108,7 @@ bool make_plan(const muon_matrix* mats, int n, int ns5_mode, Plan* P) {
   P->ns5_mode = ns5_mode;
   const size_t esize = ns5_mode == MUON_NS5_F32 ? 4 : 2;
   size_t fro_floats = 0, line_floats = 0, inv_floats = 0, osq_floats = 0;
+  P->tall_chunks = 0;
   std::map<std::pair<int, int>, std::vector<int>> open;  // (n, m) -> current group indices
   for (int i = 0; i < n; ++i) {
     MatPlan& mp = P->mats[i];
@@ -127,6 +128,7 @@ bool make_plan(const muon_matrix* mats, int n, int ns5_mode, Plan* P) {
     line_floats += (size_t)mp.line_tiles * mp.lines;
     mp.line_inv = inv_floats;
     inv_floats += mp.lines;
+    if (mp.tall) P->tall_chunks += cdiv(mp.B, TALL_CB);
     // O^2 partials of the last UPDATE: [128x256 tile][8 epilogue warps] or [64x64 tile]
     mp.osq = osq_floats;
     osq_floats += std::max((size_t)cdiv(mp.n, 128) * cdiv(mp.m, 256) * 8, (size_t)cdiv(mp.n, 64) * cdiv(mp.m, 64));
@@ -169,6 +171,8 @@ bool make_plan(const muon_matrix* mats, int n, int ns5_mode, Plan* P) {
   off = align_up(off + (size_t)std::max(n, 1) * 4, kAlign);
   P->nz = off;
   off = align_up(off + (size_t)std::max(n, 1) * 4, kAlign);
+  P->tall_ctrl = off;
+  off = align_up(off + (size_t)tall_ctrl_words(P->tall_chunks) * 4, kAlign);
   for (GroupPlan& g : P->groups) {
     const size_t xb = (size_t)g.count * g.n * g.ld_m * esize;
     const size_t sb = (size_t)g.count * g.n * g.ld_n * esize;
@@ -912,8 +916,63 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
       if ((rc = cuda_status(launch_rows(ck.w_dt, ck.g_dt, kv.first, rp, rs))) != MUON_OK) return rc;
     }
   }
-  // tall matrices: single pass, one thread-block cluster per column strip
-  if (!(g_debug_flags.load() & MUON_DEBUG_NO_CLUSTER)) {
+  const int dbg = g_debug_flags.load();
+  if (!(dbg & MUON_DEBUG_NO_CLUSTER) && !(dbg & MUON_DEBUG_TALL_CLUSTER)) {
+    // tall matrices: two row-contiguous passes, the second re-reading M from L2
+    std::map<std::pair<int, int>, std::vector<int>> tall_by_shape;
+    std::vector<int> rest;
+    for (int i : two_pass) {
+      const muon_matrix& a = mats[i];
+      const bool ok = a.rows > a.cols && a.cols % 4 == 0 && aligned(a.M, 16) && aligned(a.G, 4 * dsize(ck.g_dt)) &&
+                      aligned(a.W, 4 * dsize(ck.w_dt));
+      if (ok) tall_by_shape[std::make_pair((int)a.rows, (int)a.cols)].push_back(i);
+      else rest.push_back(i);
+    }
+    static thread_local TallParams tp;
+    unsigned* ctrl = reinterpret_cast<unsigned*>(w + P.tall_ctrl);
+    for (const auto& kv : tall_by_shape) {
+      const std::vector<int>& v = kv.second;
+      const int A = kv.first.first, Bc = kv.first.second;
+      size_t k = 0;
+      while (k < v.size()) {
+        std::memset(&tp, 0, sizeof(tp));
+        tp.rows = A;
+        tp.cols = Bc;
+        tp.ncb = cdiv(Bc, TALL_CB);
+        tp.nrb = cdiv(A, TALL_RB);
+        tp.mu = mu;
+        tp.eta = eta;
+        tp.lam = lambda;
+        tp.scale = gamma * kRmsMatch * std::sqrt((float)A);
+        int j = 0;
+        for (; k < v.size() && j < TALL_MAX_MATS; ++k) {
+          const muon_matrix& a = mats[v[k]];
+          const MatPlan& mp = P.mats[v[k]];
+          TallMat& e = tp.mat[j++];
+          e.W = a.W;
+          e.G = a.G;
+          e.M = a.M;
+          e.part = reinterpret_cast<float*>(w + P.line_part) + mp.line_part;
+          e.inv = reinterpret_cast<float*>(w + P.line_inv) + mp.line_inv;
+          e.nz = nz ? nz + v[k] : nullptr;
+        }
+        tp.nmat = j;
+        tp.nchunks = j * tp.ncb;
+        tp.lag = std::min(TALL_LAG, tp.nchunks);
+        if (2LL * tp.nchunks * tp.nrb >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
+        tp.total = 2 * tp.nchunks * tp.nrb;
+        tp.ctrl = ctrl;
+        tp.status = reinterpret_cast<unsigned int*>(w + P.status);
+        tp.timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;
+        tp.stall = (dbg & MUON_DEBUG_STALL_PRODUCER) ? 1 : 0;
+        if (cudaMemsetAsync(ctrl, 0, sizeof(unsigned) * (size_t)tall_ctrl_words(tp.nchunks), s) != cudaSuccess)
+          return MUON_ERR_CUDA;
+        if ((rc = cuda_status(launch_tall(ck.w_dt, ck.g_dt, tp, di.sms, s))) != MUON_OK) return rc;
+      }
+    }
+    two_pass.swap(rest);
+  } else if (!(dbg & MUON_DEBUG_NO_CLUSTER)) {
+    // tall matrices: single pass, one thread-block cluster per column strip
     std::map<int, std::vector<int>> tall_by_rows;
     std::vector<int> rest;
     const int stage = (int)std::max(dsize(ck.w_dt), dsize(ck.g_dt));

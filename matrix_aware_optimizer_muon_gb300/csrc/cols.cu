@@ -22,22 +22,6 @@ namespace muon {
 
 namespace {
 
-// Four consecutive elements as loaded from memory (packed), and their fp32 values.
-template <typename T> struct Raw4;
-template <> struct Raw4<float> { using type = float4; };
-template <> struct Raw4<bf16> { using type = uint2; };
-__device__ __forceinline__ float4 ldraw(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ uint2 ldraw(const bf16* p) { return *reinterpret_cast<const uint2*>(p); }
-__device__ __forceinline__ float4 ldraw_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
-__device__ __forceinline__ uint2 ldraw_stream(const bf16* p) { return __ldcs(reinterpret_cast<const uint2*>(p)); }
-__device__ __forceinline__ void cvt4(const float4& r, float v[4]) { v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w; }
-__device__ __forceinline__ void cvt4(const uint2& r, float v[4]) {
-  v[0] = __uint_as_float(r.x << 16);
-  v[1] = __uint_as_float(r.x & 0xFFFF0000u);
-  v[2] = __uint_as_float(r.y << 16);
-  v[3] = __uint_as_float(r.y & 0xFFFF0000u);
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -59,6 +59,25 @@ __device__ __forceinline__ void st4(bf16* p, const float v[4]) {
   *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
 }
 
+// Packed 4-element loads: the raw registers as loaded, converted later.  Kernels
+// issue every raw load of a thread first and convert afterwards, so that a
+// thread's DRAM requests are all in flight together rather than one round trip
+// per chunk.
+template <typename T> struct Raw4;
+template <> struct Raw4<float> { using type = float4; };
+template <> struct Raw4<bf16> { using type = uint2; };
+__device__ __forceinline__ float4 ldraw(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ uint2 ldraw(const bf16* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ float4 ldraw_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ uint2 ldraw_stream(const bf16* p) { return __ldcs(reinterpret_cast<const uint2*>(p)); }
+__device__ __forceinline__ void cvt4(const float4& r, float v[4]) { v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w; }
+__device__ __forceinline__ void cvt4(const uint2& r, float v[4]) {
+  v[0] = __uint_as_float(r.x << 16);
+  v[1] = __uint_as_float(r.x & 0xFFFF0000u);
+  v[2] = __uint_as_float(r.y << 16);
+  v[3] = __uint_as_float(r.y & 0xFFFF0000u);
+}
+
 // element-wise (unaligned / ragged) access
 template <typename T> __device__ __forceinline__ float ld1(const T* p) { return to_f32(*p); }
 template <typename T> __device__ __forceinline__ void st1(T* p, float v) { *p = from_f32<T>(v); }

@@ -72,21 +72,47 @@ ew_tile_kernel(const __grid_constant__ EwParams p) {
   }
 
   // ---- load (and momentum) ----
+  if (vec) {
+    // every row's loads are issued before any is used: one DRAM round trip per tile
+    float4 mr[RPT];
+    typename Raw4<GT>::type gr[kMom ? RPT : 1];
+    typename Raw4<WT>::type wr[kApply ? RPT : 1];
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    const int r = r0 + warp + (EW_THREADS / 32) * i;
-    const bool rok = r < rows;
-    const size_t off = (size_t)r * (size_t)cols + (size_t)cb;
-    if (rok && vec) {
-      ld4(Mp + off, v[i]);
-      if constexpr (kMom) {
-        float g[4];
-        ld4_stream(reinterpret_cast<const GT*>(mt.G) + off, g);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[i][j] = p.mu * v[i][j] + g[j];
+    for (int i = 0; i < RPT; ++i) {
+      const int r = r0 + warp + (EW_THREADS / 32) * i;
+      const size_t off = (size_t)r * (size_t)cols + (size_t)cb;
+      if (r < rows) {
+        mr[i] = ldraw(Mp + off);
+        if constexpr (kMom) gr[i] = ldraw_stream(reinterpret_cast<const GT*>(mt.G) + off);
+        if constexpr (kApply) wr[i] = ldraw(reinterpret_cast<const WT*>(mt.W) + off);
       }
-      if constexpr (kApply) ld4(reinterpret_cast<const WT*>(mt.W) + off, w[i]);
-    } else {
+    }
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int r = r0 + warp + (EW_THREADS / 32) * i;
+      if (r < rows) {
+        cvt4(mr[i], v[i]);
+        if constexpr (kMom) {
+          float g[4];
+          cvt4(gr[i], g);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[i][j] = p.mu * v[i][j] + g[j];
+        }
+        if constexpr (kApply) cvt4(wr[i], w[i]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[i][j] = 0.f;
+          if constexpr (kApply) w[i][j] = 0.f;
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int r = r0 + warp + (EW_THREADS / 32) * i;
+      const bool rok = r < rows;
+      const size_t off = (size_t)r * (size_t)cols + (size_t)cb;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const bool ok = rok && (cb + j < cols);
@@ -267,26 +293,51 @@ rows_kernel(const __grid_constant__ RowsParams p) {
 
   float v[CPT][4], w[CPT][4];
   float ss = 0.f;
+  if (mt.vec) {
+    // every chunk's loads are issued before any is used: one DRAM round trip per row
+    float4 mr[CPT];
+    typename Raw4<GT>::type gr[CPT];
+    typename Raw4<WT>::type wr[CPT];
 #pragma unroll
-  for (int k = 0; k < CPT; ++k) {
-    const int c = (threadIdx.x + k * blockDim.x) * 4;
-    if (mt.vec && c + 4 <= cols) {
+    for (int k = 0; k < CPT; ++k) {
+      const int c = (threadIdx.x + k * blockDim.x) * 4;
+      if (c + 4 <= cols) {
+        mr[k] = ldraw(Mp + c);
+        gr[k] = ldraw_stream(Gp + c);
+        wr[k] = ldraw(Wp + c);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+      const int c = (threadIdx.x + k * blockDim.x) * 4;
       float g[4];
-      ld4(Mp + c, v[k]);
-      ld4_stream(Gp + c, g);
-      ld4(Wp + c, w[k]);
+      if (c + 4 <= cols) {
+        cvt4(mr[k], v[k]);
+        cvt4(gr[k], g);
+        cvt4(wr[k], w[k]);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[k][j] = p.mu * v[k][j] + g[j];
-    } else {
+        for (int j = 0; j < 4; ++j) v[k][j] = g[j] = w[k][j] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[k][j] = p.mu * v[k][j] + g[j];
+        ss = fmaf(v[k][j], v[k][j], ss);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+      const int c = (threadIdx.x + k * blockDim.x) * 4;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const bool ok = c + j < cols;
         v[k][j] = ok ? p.mu * Mp[c + j] + ld1(Gp + c + j) : 0.f;
         w[k][j] = ok ? ld1(Wp + c + j) : 0.f;
       }
-    }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) ss = fmaf(v[k][j], v[k][j], ss);
+      for (int j = 0; j < 4; ++j) ss = fmaf(v[k][j], v[k][j], ss);
+    }
   }
   const float inv = inv_norm_from_sumsq(block_sum(ss, red));
   if (mt.nz && threadIdx.x == 0 && inv > 0.f) atomicAdd(mt.nz, 1);   // telemetry: nonzero rows
@@ -323,17 +374,43 @@ apply_kernel(const __grid_constant__ ApplyParams p) {
   const long long e0 = (long long)(b - mt.block_begin) * APPLY_CHUNK;
   WT* Wp = reinterpret_cast<WT*>(mt.W);
   const UT* Up = reinterpret_cast<const UT*>(mt.U);
+  constexpr int KC = APPLY_CHUNK / (256 * 4);
+  if (mt.vec) {
+    // all loads of the block first, then the updates: one DRAM round trip per thread
+    typename Raw4<WT>::type wr[KC];
+    typename Raw4<UT>::type ur[KC];
 #pragma unroll
-  for (int k = 0; k < APPLY_CHUNK / (256 * 4); ++k) {
-    const long long e = e0 + (long long)(k * 256 + threadIdx.x) * 4;
-    if (mt.vec && e + 4 <= mt.numel) {
-      float w[4], u[4], o[4];
-      ld4(Wp + e, w);
-      ld4_stream(Up + e, u);
+    for (int k = 0; k < KC; ++k) {
+      const long long e = e0 + (long long)(k * 256 + threadIdx.x) * 4;
+      if (e + 4 <= mt.numel) {
+        wr[k] = ldraw(Wp + e);
+        ur[k] = ldraw_stream(Up + e);
+      }
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o[j] = w[j] - p.eta * (mt.scale * u[j] + p.lam * w[j]);
-      st4(Wp + e, o);
-    } else {
+    for (int k = 0; k < KC; ++k) {
+      const long long e = e0 + (long long)(k * 256 + threadIdx.x) * 4;
+      if (e + 4 <= mt.numel) {
+        float w[4], u[4], o[4];
+        cvt4(wr[k], w);
+        cvt4(ur[k], u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = w[j] - p.eta * (mt.scale * u[j] + p.lam * w[j]);
+        st4(Wp + e, o);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (e + j < mt.numel) {
+            const float w = ld1(Wp + e + j), u = ld1(Up + e + j);
+            st1(Wp + e + j, w - p.eta * (mt.scale * u + p.lam * w));
+          }
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+      const long long e = e0 + (long long)(k * 256 + threadIdx.x) * 4;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (e + j < mt.numel) {
@@ -430,6 +507,22 @@ __global__ void nz_rms_kernel(const __grid_constant__ NzRmsParams p) {
 // (n x m, leading dimension ld).  64 x 64 tiles of O pass through shared memory so
 // that a tall W (m x n, W[c][r] = update of O[r][c]) is read and written along its
 // rows too.
+// Element idx of a 64 x 64 tile of O (n x m) and the W element it updates:
+// W is n x m (wide; consecutive idx walk a row of W and of O) or m x n (tall;
+// consecutive idx walk a row of W, a column of O).
+__device__ __forceinline__ void applyws_coords(bool tall, int idx, int r0, int c0, int n, int m, int& rr,
+                                               int& cc, size_t& widx) {
+  if (!tall) {
+    rr = idx / APPLYWS_TILE;
+    cc = idx % APPLYWS_TILE;
+    widx = (size_t)(r0 + rr) * m + (c0 + cc);
+  } else {
+    cc = idx / APPLYWS_TILE;
+    rr = idx % APPLYWS_TILE;
+    widx = (size_t)(c0 + cc) * n + (r0 + rr);
+  }
+}
+
 template <typename WT, typename OT>
 __global__ void __launch_bounds__(256)
 apply_ws_kernel(const __grid_constant__ ApplyWsParams p) {
@@ -447,36 +540,46 @@ apply_ws_kernel(const __grid_constant__ ApplyWsParams p) {
   const int n = mt.n, m = mt.m;
   const OT* O = reinterpret_cast<const OT*>(mt.O);
   const bf16* L = reinterpret_cast<const bf16*>(mt.O_lo);
-  for (int idx = threadIdx.x; idx < APPLYWS_TILE * APPLYWS_TILE; idx += blockDim.x) {
-    const int rr = idx / APPLYWS_TILE, cc = idx % APPLYWS_TILE;
-    const int r = r0 + rr, c = c0 + cc;
-    float v = 0.f;
-    if (r < n && c < m) {
-      const size_t off = (size_t)r * mt.ld + c;
-      v = to_f32(O[off]);
-      if (L) v += __bfloat162float(L[off]);
+  constexpr int PER = APPLYWS_TILE * APPLYWS_TILE / 256;   // elements per thread (256 threads)
+  {
+    float ov[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int idx = threadIdx.x + q * 256;
+      const int r = r0 + idx / APPLYWS_TILE, c = c0 + idx % APPLYWS_TILE;
+      ov[q] = 0.f;
+      if (r < n && c < m) {
+        const size_t off = (size_t)r * mt.ld + c;
+        ov[q] = to_f32(O[off]);
+        if (L) ov[q] += __bfloat162float(L[off]);
+      }
     }
-    t[rr][cc] = v;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int idx = threadIdx.x + q * 256;
+      t[idx / APPLYWS_TILE][idx % APPLYWS_TILE] = ov[q];
+    }
   }
   __syncthreads();
   const float sc = p.scale[mt.scale_index];
   WT* W = reinterpret_cast<WT*>(mt.W);
-  for (int idx = threadIdx.x; idx < APPLYWS_TILE * APPLYWS_TILE; idx += blockDim.x) {
+  // every element's W load is issued before the first store (one DRAM round trip)
+  float wv[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int idx = threadIdx.x + q * 256;
     int rr, cc;
     size_t widx;
-    if (!mt.tall) {          // W is n x m: consecutive threads walk a row of W and of O
-      rr = idx / APPLYWS_TILE;
-      cc = idx % APPLYWS_TILE;
-      widx = (size_t)(r0 + rr) * m + (c0 + cc);
-    } else {                 // W is m x n: consecutive threads walk a row of W (a column of O)
-      cc = idx / APPLYWS_TILE;
-      rr = idx % APPLYWS_TILE;
-      widx = (size_t)(c0 + cc) * n + (r0 + rr);
-    }
-    if (r0 + rr < n && c0 + cc < m) {
-      const float w = ld1(W + widx);
-      st1(W + widx, w - p.eta * (sc * t[rr][cc] + p.lam * w));
-    }
+    applyws_coords(mt.tall, idx, r0, c0, n, m, rr, cc, widx);
+    wv[q] = (r0 + rr < n && c0 + cc < m) ? ld1(W + widx) : 0.f;
+  }
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int idx = threadIdx.x + q * 256;
+    int rr, cc;
+    size_t widx;
+    applyws_coords(mt.tall, idx, r0, c0, n, m, rr, cc, widx);
+    if (r0 + rr < n && c0 + cc < m) st1(W + widx, wv[q] - p.eta * (sc * t[rr][cc] + p.lam * wv[q]));
   }
 }
 

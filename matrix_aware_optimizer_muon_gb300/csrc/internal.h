@@ -97,6 +97,40 @@ struct ColsParams {
   float mu, eta, lam;
 };
 
+// RowNorm step for tall matrices as two row-contiguous passes (tall.cu): chunks
+// of TALL_CB columns x all rows, tiles of TALL_RB rows of a chunk.  Every matrix
+// of one launch has the same shape.
+constexpr int TALL_RB = 128;
+constexpr int TALL_CB = 128;
+constexpr int TALL_MAX_MATS = 128;
+constexpr int TALL_LAG = 4;   // chunks between a chunk's first and second pass in ticket order
+struct TallMat {
+  void* W;
+  const void* G;
+  float* M;
+  float* part;             // [ceil(rows / TALL_RB)][cols] tile column sums of squares
+  float* inv;              // [cols] inverse column norms
+  int* nz;                 // optional: count of nonzero columns (update-RMS telemetry)
+};
+struct TallParams {
+  TallMat mat[TALL_MAX_MATS];
+  int nmat;
+  int rows, cols;          // shape shared by every matrix of the launch
+  int ncb;                 // column blocks per matrix
+  int nrb;                 // row blocks (tiles) per chunk
+  int nchunks;             // nmat * ncb
+  int lag;                 // min(TALL_LAG, nchunks)
+  int total;               // tickets: 2 * nchunks * nrb
+  float mu, eta, lam, scale;
+  unsigned* ctrl;          // [0] ticket, [1 + c] tiles done, [1 + NC + c] ready, [1 + 2 NC] abort
+  unsigned int* status;    // workspace status word
+  unsigned long long timeout_ns;
+  int stall;               // test hook: publish no column norms, so that pass 2 times out
+};
+
+// Status-word bit set by a kernel whose bounded wait expired.
+constexpr uint32_t DEV_TIMEOUT = 1u;
+
 // apply from a given direction U
 constexpr int APPLY_MAX_MATS = 128;
 constexpr int APPLY_CHUNK = 4096;  // elements per CTA
@@ -282,6 +316,8 @@ struct Plan {
   size_t osq_part;         // partial sums of O^2 (telemetry / Eq. (6))
   size_t scale;            // per matrix Eq. (6) scale
   size_t nz;               // per matrix nonzero-line counts (int)
+  size_t tall_ctrl;        // control words of the tall-matrix RowNorm kernel (unsigned)
+  int tall_chunks;         // column blocks over all tall matrices
   size_t total;
 };
 
@@ -290,6 +326,8 @@ cudaError_t launch_ew(int mode, int w_dt, int g_dt, int x_dt, const EwParams& p,
 cudaError_t launch_rows(int w_dt, int g_dt, int max_cols, const RowsParams& p, cudaStream_t s);
 cudaError_t launch_apply(int w_dt, int u_dt, const ApplyParams& p, cudaStream_t s);
 cudaError_t launch_cols(int w_dt, int g_dt, int cw, const ColsParams& p, cudaStream_t s);
+cudaError_t launch_tall(int w_dt, int g_dt, const TallParams& p, int num_sms, cudaStream_t s);
+int tall_ctrl_words(int nchunks);
 int cols_cluster_size();
 int cols_strip_width(int max_rows, int stage_elem_bytes);
 cudaError_t launch_fro_final(const FroFinalParams& p, cudaStream_t s);
@@ -311,6 +349,7 @@ namespace muon {
 // Kernel parameters are limited to 32764 bytes.
 static_assert(sizeof(EwParams) < 32000, "EwParams too large");
 static_assert(sizeof(RowsParams) < 32000, "RowsParams too large");
+static_assert(sizeof(TallParams) < 32000, "TallParams too large");
 static_assert(sizeof(ApplyParams) < 32000, "ApplyParams too large");
 static_assert(sizeof(FroFinalParams) < 32000, "FroFinalParams too large");
 static_assert(sizeof(LineFinalParams) < 32000, "LineFinalParams too large");

@@ -43,7 +43,6 @@ constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int EPI_CHUNKS = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per epilogue warp
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-constexpr uint32_t DEV_TIMEOUT = 1u;
 
 struct Tile {
   int g, mat, tm, tn;

@@ -122,21 +122,29 @@ def test_apply_parity(wdt, udt):
 # ---------------------------------------------------------------------------
 # RowNorm step (fused momentum + RowNorm + apply), wide and tall, ragged
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("path", ["cluster", "two_pass"])
+# Tall-matrix routes of a RowNorm step: the default two row-contiguous passes with
+# the second re-reading M from L2, the single-pass cluster kernel, the plain two-pass kernels.
+TALL_PATHS = {"l2pass": 0, "cluster": mm.MUON_DEBUG_TALL_CLUSTER, "two_pass": mm.MUON_DEBUG_NO_CLUSTER}
+
+
+@pytest.mark.parametrize("path", list(TALL_PATHS))
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
 def test_rownorm_step_parity(dt, path):
-    """Wide rows (single pass), tall columns (cluster single pass, or the two-pass
-    form), ragged and degenerate shapes; (40000, 8) takes 16-column strips and
-    (70000, 8) is too tall for the cluster's shared memory."""
+    """Wide rows (single pass) and tall columns on each tall route, ragged and degenerate
+    shapes.  For the L2 two-pass kernel: (4608, 1536) has 12 column blocks x 36 row blocks
+    (more chunks than the pass-2 lag), the two (1000, 300) share one launch with a ragged
+    last column block and row block, (40000, 8) has 313 row blocks.  For the cluster
+    kernel (40000, 8) takes 16-column strips and (70000, 8) is too tall for its shared
+    memory.  (13, 7) and (517, 1) have B % 4 != 0 and take the plain two-pass kernels."""
     shapes = [(256, 1024), (300, 1000), (1000, 300), (1536, 1536), (7, 13), (13, 7), (1, 517), (517, 1),
-              (3, 20000), (129, 129), (4608, 1536), (300, 36), (40000, 8), (70000, 8), (33, 4)]
+              (3, 20000), (129, 129), (4608, 1536), (300, 36), (40000, 8), (70000, 8), (33, 4), (1000, 300)]
     W0, Gs = inputs(shapes, dt, dt, 2)
     M0 = rand_M(shapes, seed=8, zero_line=True)
     W = [to_dev(w, dt) for w in W0]
     M = [to_dev(m, "f32") for m in M0]
     G = [to_dev(g, dt) for g in Gs[1]]
     ws = mm.alloc_workspace(shapes)
-    mm.muon_debug_set(mm.MUON_DEBUG_NO_CLUSTER if path == "two_pass" else 0, 0)
+    mm.muon_debug_set(TALL_PATHS[path], 0)
     try:
         br = mm.muon_periodic_step(W, G, M, 1, ws, K=3)
     finally:
@@ -383,6 +391,34 @@ def test_stalled_producer_times_out_and_context_survives():
     assert rel_fro(to_np(O[0]), ref) <= TOL_NS5_BF16
 
 
+def test_tall_pass2_wait_times_out_and_context_survives():
+    """The tall-matrix kernel publishes no column norms under the stall hook: its pass-2
+    waits expire, the status word reports it, and the next step on the same context is exact."""
+    shapes = [(1000, 300), (4608, 1536)]
+    W0, Gs = inputs(shapes, "bf16", "bf16", 2)
+    M0 = rand_M(shapes, seed=14)
+    W = [to_dev(w, "bf16") for w in W0]
+    M = [to_dev(m, "f32") for m in M0]
+    G = [to_dev(g, "bf16") for g in Gs[1]]
+    ws = mm.alloc_workspace(shapes)
+    mm.muon_debug_set(mm.MUON_DEBUG_STALL_PRODUCER, 50)
+    try:
+        mm.muon_periodic_step(W, G, M, 1, ws)
+        assert mm.muon_check_status(ws) == mm.MUON_ERR_TIMEOUT
+    finally:
+        mm.muon_debug_set(0, 0)
+    W = [to_dev(w, "bf16") for w in W0]
+    M = [to_dev(m, "f32") for m in M0]
+    mm.muon_periodic_step(W, G, M, 1, ws)
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(shapes):
+        refW, refM, _ = muon_ref.periodic_step(W0[i], M0[i], Gs[1][i], 1, 3, 0.15, 0.95, 0.02, 0.01)
+        assert_f32_close(to_np(M[i]), refM, what=f"M {shapes[i]}")
+        terms = apply_terms(W0[i], muon_ref.rownorm(refM), muon_ref.update_scale(a, b, False, 0.15), 0.02, 0.01)
+        assert_bf16_close(to_np(W[i]), refW, terms, what=f"W {shapes[i]}")
+
+
 def test_rownorm_overlap_matches_serial():
     """Wide-row kernels on the library's second stream give the same bits as running serially."""
     shapes = [(1536, 1536), (1536, 6144), (4608, 1536), (6144, 1536), (300, 1000), (1000, 300)]
@@ -475,7 +511,7 @@ def test_update_norm_refresh_step_parity(dt, mode):
         assert abs(muon_ref.rms(got_dir) - 0.2) <= tol * 0.2 + np.linalg.norm(np.abs(refW)) * ulp / 0.02 / math.sqrt(a * b)
 
 
-@pytest.mark.parametrize("path", ["cluster", "two_pass"])
+@pytest.mark.parametrize("path", list(TALL_PATHS))
 def test_update_rms_telemetry(path):
     shapes = [(256, 1024), (1000, 300), (4608, 1536), (1536, 6144), (300, 36), (13, 7), (0, 5), (40000, 8)]
     W0, Gs = inputs(shapes, "bf16", "bf16", 2)
@@ -490,7 +526,7 @@ def test_update_rms_telemetry(path):
     M = [to_dev(m, "f32") for m in M0]
     ws = mm.alloc_workspace(shapes)
     rms = torch.full((len(shapes),), -1.0, device=dev())
-    mm.muon_debug_set(mm.MUON_DEBUG_NO_CLUSTER if path == "two_pass" else 0, 0)
+    mm.muon_debug_set(TALL_PATHS[path], 0)
     try:
         # RowNorm step (scale_mode update_norm equals Eq. (7) when no line is zero; here some are)
         G = [to_dev(g, "bf16") for g in Gs[1]]
