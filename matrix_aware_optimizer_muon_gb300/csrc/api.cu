@@ -958,7 +958,8 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
         }
         tp.nmat = j;
         tp.nchunks = j * tp.ncb;
-        tp.lag = std::min(TALL_LAG, tp.nchunks);
+        const int lag = (int)std::lround(TALL_LAG_BYTES / ((double)A * TALL_CB * 4.0));
+        tp.lag = std::min(std::max(2, std::min(lag, 32)), tp.nchunks);
         if (2LL * tp.nchunks * tp.nrb >= (1LL << 31)) return MUON_ERR_UNSUPPORTED;
         tp.total = 2 * tp.nchunks * tp.nrb;
         tp.ctrl = ctrl;

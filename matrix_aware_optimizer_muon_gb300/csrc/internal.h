@@ -100,10 +100,14 @@ struct ColsParams {
 // RowNorm step for tall matrices as two row-contiguous passes (tall.cu): chunks
 // of TALL_CB columns x all rows, tiles of TALL_RB rows of a chunk.  Every matrix
 // of one launch has the same shape.
-constexpr int TALL_RB = 128;
+constexpr int TALL_RB = 256;
 constexpr int TALL_CB = 128;
 constexpr int TALL_MAX_MATS = 128;
-constexpr int TALL_LAG = 4;   // chunks between a chunk's first and second pass in ticket order
+// New momentum (bytes) that waits in L2 between a chunk's first and second pass: the
+// pass-2 lag in chunks is this over a chunk's A x TALL_CB x 4 bytes, in [2, 32].
+// Measured on the 1.3B set: a shorter lag makes pass-2 tiles wait, a longer one
+// spills the momentum out of L2.
+constexpr double TALL_LAG_BYTES = 32e6;
 struct TallMat {
   void* W;
   const void* G;
@@ -119,7 +123,7 @@ struct TallParams {
   int ncb;                 // column blocks per matrix
   int nrb;                 // row blocks (tiles) per chunk
   int nchunks;             // nmat * ncb
-  int lag;                 // min(TALL_LAG, nchunks)
+  int lag;                 // chunks between a chunk's pass 1 and pass 2 in ticket order (<= nchunks)
   int total;               // tickets: 2 * nchunks * nrb
   float mu, eta, lam, scale;
   unsigned* ctrl;          // [0] ticket, [1 + c] tiles done, [1 + NC + c] ready, [1 + 2 NC] abort

@@ -3,16 +3,16 @@
 // paragraph: tall matrices reduce per-column norm scalars) as two row-contiguous
 // passes whose second pass finds the new momentum still in L2.
 //
-// A chunk is one 128-column block of one matrix, all A rows.  A tile is 128 rows
+// A chunk is one 128-column block of one matrix, all A rows.  A tile is 256 rows
 // of a chunk.  Pass 1 of a tile computes M <- mu*M + G, stores M and writes the
 // tile's 128 column sums of squares; the CTA that completes a chunk's last
 // pass-1 tile adds the chunk's tile sums in row-block order and publishes the
 // 128 inverse column norms.  Pass 2 of a tile re-reads M and applies
 //   W <- W - eta*(s*M/||column|| + lambda*W).
 // Persistent CTAs take tiles from one atomic ticket counter in a fixed order in
-// which pass 2 of chunk c comes LAG chunks after its pass 1: pass-1 tiles never
-// wait, and by the time a pass-2 tile is handed out its chunk is normally
-// finished, while the chunk's new momentum (a few MB) is still in L2.  HBM
+// which pass 2 of chunk c comes a few chunks (about 32 MB of momentum) after its
+// pass 1: pass-1 tiles never wait, and by the time a pass-2 tile is handed out
+// its chunk is normally finished, while the chunk's new momentum is still in L2.  HBM
 // traffic is then G 2 + M 4 + M 4 + W 2 + W 2 = 14 bytes per element, with
 // every access a 512-byte (M) or 256-byte (G, W) row segment.
 //
@@ -35,7 +35,7 @@ namespace {
 
 constexpr int TL_NT = 256;                     // threads per CTA: 8 warps
 constexpr int TL_WARPS = TL_NT / 32;
-constexpr int TL_RPT = TALL_RB / TL_WARPS;     // rows per thread per tile (16)
+constexpr int TL_RPT = TALL_RB / TL_WARPS;     // rows per thread per tile (32)
 constexpr int TL_U = 4;                        // rows in flight per thread (measured best with 3 CTAs/SM)
 static_assert(TALL_CB == 128, "one warp covers 128 columns (4 per lane)");
 static_assert(TL_RPT % TL_U == 0, "tile rows split into whole batches");
