@@ -105,9 +105,12 @@ constexpr int TALL_CB = 128;
 constexpr int TALL_MAX_MATS = 128;
 // New momentum (bytes) that waits in L2 between a chunk's first and second pass: the
 // pass-2 lag in chunks is this over a chunk's A x TALL_CB x 4 bytes, in [2, 32].
-// Measured on the 1.3B set: a shorter lag makes pass-2 tiles wait, a longer one
-// spills the momentum out of L2.
-constexpr double TALL_LAG_BYTES = 32e6;
+// Measured on the 1.3B set (24 / 32 / 48 / 64 MB): a shorter lag makes pass-2 tiles
+// wait, a longer one spills the momentum out of L2.
+#ifndef MUON_TALL_LAG_BYTES
+#define MUON_TALL_LAG_BYTES 48e6
+#endif
+constexpr double TALL_LAG_BYTES = MUON_TALL_LAG_BYTES;
 struct TallMat {
   void* W;
   const void* G;

@@ -10,7 +10,7 @@
 // 128 inverse column norms.  Pass 2 of a tile re-reads M and applies
 //   W <- W - eta*(s*M/||column|| + lambda*W).
 // Persistent CTAs take tiles from one atomic ticket counter in a fixed order in
-// which pass 2 of chunk c comes a few chunks (about 32 MB of momentum) after its
+// which pass 2 of chunk c comes a few chunks (about 48 MB of momentum) after its
 // pass 1: pass-1 tiles never wait, and by the time a pass-2 tile is handed out
 // its chunk is normally finished, while the chunk's new momentum is still in L2.  HBM
 // traffic is then G 2 + M 4 + M 4 + W 2 + W 2 = 14 bytes per element, with
@@ -67,6 +67,31 @@ __device__ __forceinline__ TallTicket tall_decode(int t, int NC, int T, int L) {
 }
 
 __device__ __forceinline__ float4 ld_cg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+// L2 eviction priority: the new momentum written by pass 1 is kept (evict-last)
+// until pass 2 reads it back, and that read marks it evict-first.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ float4 ld_cg4_hint(const float* a, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(a), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st4_hint(float* a, const float v[4], uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(a), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+               "f"(v[3]), "l"(pol)
+               : "memory");
+}
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
@@ -131,7 +156,7 @@ __global__ void __launch_bounds__(TL_NT, sizeof(WT) + sizeof(GT) <= 4 ? 3 : 2) t
             v[1] = p.mu * mr[u].y + g[1];
             v[2] = p.mu * mr[u].z + g[2];
             v[3] = p.mu * mr[u].w + g[3];
-            st4(M + (size_t)r * B + c, v);
+            st4_hint(M + (size_t)r * B + c, v, l2_policy_evict_last());
 #pragma unroll
             for (int j = 0; j < 4; ++j) cs[j] = fmaf(v[j], v[j], cs[j]);
           }
@@ -211,7 +236,7 @@ __global__ void __launch_bounds__(TL_NT, sizeof(WT) + sizeof(GT) <= 4 ? 3 : 2) t
           const int r = r0 + warp + TL_WARPS * (b * TL_U + u);
           if (r < A && colok) {
             const size_t off = (size_t)r * B + c;
-            mr[u] = ld_cg4(M + off);
+            mr[u] = ld_cg4_hint(M + off, l2_policy_evict_first());
             wr[u] = ldraw(W + off);
           }
         }
