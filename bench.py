@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--K", type=int, default=0,
+                    help="override the schedule period K (1 = vanilla Muon: every step is a refresh)")
     ap.add_argument("--matrices", type=int, default=0,
                     help="keep only the first N matrices of the set (small cases for profiling)")
     return ap.parse_args()
@@ -212,6 +214,8 @@ def select_workload(args):
     wl = WORKLOADS[args.workload]
     if args.matrices and args.matrices < len(wl.matrices):
         wl = dataclasses.replace(wl, key=f"{wl.key}[:{args.matrices}]", matrices=wl.matrices[:args.matrices])
+    if args.K and args.K != wl.K:
+        wl = dataclasses.replace(wl, key=f"{wl.key}/K={args.K}", K=args.K)
     return wl
 
 
@@ -331,7 +335,8 @@ def run_ours(args, torch):
     period_ms = max_over_ranks(torch, dist, period_ms, device)
     refresh_ms = statistics.mean(s[0].elapsed_time(s[2]) for s in evs)
     ns5_ms = statistics.mean(s[1].elapsed_time(s[2]) for s in evs)
-    rownorm_ms = statistics.mean(s[3].elapsed_time(s[4]) for s in evs)   # the last RowNorm step of each period
+    has_rn = wl.K > 1   # K = 1 (vanilla Muon) has no RowNorm steps
+    rownorm_ms = statistics.mean(s[3].elapsed_time(s[4]) for s in evs) if has_rn else None   # last RowNorm step of each period
     gpu_launches = launches[0] // args.steps
 
     flops = ns5_flops(shapes)
@@ -340,7 +345,7 @@ def run_ours(args, torch):
     pk, pk_src = peaks()
     ns5_tflops = flops / (ns5_ms * 1e-3) / 1e12
     ns5_exec_tflops = flops_exec / (ns5_ms * 1e-3) / 1e12
-    rn_gbs = rn_bytes / (rownorm_ms * 1e-3) / 1e9
+    rn_gbs = rn_bytes / (rownorm_ms * 1e-3) / 1e9 if has_rn else None
     peak_tc = pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
     peak_hbm = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
     n_ns5_launches = 15 * max(1, math.ceil(len(wl.shape_groups()) / 8))
@@ -354,12 +359,14 @@ def run_ours(args, torch):
         "data": "synthetic",
         "config": {"workload": wl.key, "matrices": len(shapes), "params": wl.n_params,
                    "K": wl.K, "gamma": wl.gamma, "mu": wl.mu, "eta": wl.eta, "lambda": wl.lam,
-                   "step": f"one K={wl.K} period: 1 NS5 refresh + {wl.K - 1} RowNorm optimizer steps; value = period/{wl.K}",
+                   "step": (f"one K={wl.K} period: 1 NS5 refresh + {wl.K - 1} RowNorm optimizer steps; value = period/{wl.K}"
+                            if wl.K > 1 else "vanilla Muon (K=1): every optimizer step is an NS5 refresh"),
                    "l2": f"inputs larger than L2 (W+G+M {tot * (wb + gb + 4) / 1e9:.1f} GB vs 129 MB L2), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "refresh_ms": round(refresh_ms, 4), "ns5_ms": round(ns5_ms, 4), "rownorm_ms": round(rownorm_ms, 4),
+        "refresh_ms": round(refresh_ms, 4), "ns5_ms": round(ns5_ms, 4),
+        "rownorm_ms": round(rownorm_ms, 4) if has_rn else None,
         "ns5_tflops": round(ns5_tflops, 1), "ns5_tflops_executed": round(ns5_exec_tflops, 1),
-        "rownorm_gbs": round(rn_gbs, 1),
+        "rownorm_gbs": round(rn_gbs, 1) if has_rn else None,
         "roofline": {"kernel": "ns_tc_kernel (Newton-Schulz GEMMs)", "bound": "tensor",
                      "achieved": round(ns5_tflops, 1), "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": round(ns5_tflops / peak_tc, 4), "traffic": ns5_traffic,
@@ -370,7 +377,8 @@ def run_ours(args, torch):
                      "flops_per_refresh": flops, "launches_per_refresh": n_ns5_launches},
         "rownorm_roofline": {"bound": "hbm", "achieved": round(rn_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                              "frac": round(rn_gbs / peak_hbm, 4), "bytes_per_step": rn_bytes,
-                             "peak_source": f"{pk_src} hbm_gbs", "frac_of_nominal_8000": round(rn_gbs / 8000.0, 4)},
+                             "peak_source": f"{pk_src} hbm_gbs", "frac_of_nominal_8000": round(rn_gbs / 8000.0, 4)}
+        if has_rn else None,
         "gpu_launches": gpu_launches,
         "clocks": clk,
         "wall_s": round(wall, 3),
