@@ -412,9 +412,10 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
         prm.c = kNsC;
         prm.first_iter = iter == 0;
         prm.last_iter = (iter == kNsSteps - 1) && kind == GEMM_UPDATE;
-        // Late iterations (X already near its fixed band) take a*X inside the
-        // tensor-core product; the first NS_LO_ITERS + 1 keep a*X in fp32.
-        prm.fold_a = tcmode && iter > NS_LO_ITERS && kind != GEMM_GRAM;
+        // Iterations after the first take a*X_hi inside the tensor-core product
+        // ((B + aI) X_hi with B + aI rounded to bf16); the epilogue adds a*X_lo where
+        // the residual is carried.  The first iteration takes a*X0 from the fp32 M.
+        prm.fold_a = tcmode && iter >= 1 && kind != GEMM_GRAM;
         prm.inv_norm = inv_norm_all + gbase[ch.first];
         prm.dst_mode = dst_mode;
         prm.dst_dtype = dst_dtype;

@@ -229,7 +229,7 @@ struct LineFinalParams {
 // ---------------------------------------------------------------------------
 enum GemmKind : int { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_UPDATE = 2 };
 enum NsFlags : int { NS_TALL = 1, NS_MVEC = 2, NS_WVEC = 4 };
-// Iterations 1..NS_LO_ITERS add a bf16 residual to the bf16 X in the a*X term
+// Iterations 1..NS_LO_ITERS add a*X_lo, the bf16 residual of X, to (B + aI) X_hi
 // (X carried with ~16 significant bits where the small singular directions are
 // still far below the element magnitudes).
 constexpr int NS_LO_ITERS = 2;

@@ -204,8 +204,18 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
     const bool full = c0 + 32 <= m;
     float x[32];
     if (p.fold_a) {
+      // a*X_hi is already in the accumulator ((B + aI) X_hi); the residual X_lo,
+      // where it is carried, adds a*X_lo here
+      if (G.lo_in && in.ok) {
+        unpack_bf16x32(in.w + 16, x);
+      } else if (G.lo_in) {
+        const bf16* Lin = reinterpret_cast<const bf16*>(G.lo_in) + (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = 0.f;   // a*X is already in the accumulator
+        for (int j = 0; j < 32; ++j) x[j] = (c0 + j < m) ? __bfloat162float(Lin[c0 + j]) : 0.f;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = 0.f;
+      }
     } else if (in.ok && p.first_iter) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(in.w[j]);

@@ -419,6 +419,32 @@ def test_tall_pass2_wait_times_out_and_context_survives():
         assert_bf16_close(to_np(W[i]), refW, terms, what=f"W {shapes[i]}")
 
 
+def test_tall_matrices_spanning_several_launches():
+    """130 tall matrices of one shape take two launches of the tall-matrix kernel (at most
+    128 per launch), reusing its control words; each matrix has two ragged row tiles."""
+    shapes = [(260, 8)] * 130 + [(520, 12)] * 2
+    W0, Gs = inputs(shapes, "bf16", "bf16", 2)
+    M0 = rand_M(shapes, seed=15)
+    runs = []
+    for _ in range(2):
+        W = [to_dev(w, "bf16") for w in W0]
+        M = [to_dev(m, "f32") for m in M0]
+        G = [to_dev(g, "bf16") for g in Gs[1]]
+        ws = mm.alloc_workspace(shapes)
+        mm.muon_periodic_step(W, G, M, 1, ws)
+        assert mm.muon_check_status(ws) == mm.MUON_OK
+        torch.cuda.synchronize()
+        runs.append((W, M))
+    W, M = runs[0]
+    for i, (a, b) in enumerate(shapes):
+        refW, refM, _ = muon_ref.periodic_step(W0[i], M0[i], Gs[1][i], 1, 3, 0.15, 0.95, 0.02, 0.01)
+        assert_f32_close(to_np(M[i]), refM, what=f"M {i}")
+        terms = apply_terms(W0[i], muon_ref.rownorm(refM), muon_ref.update_scale(a, b, False, 0.15), 0.02, 0.01)
+        assert_bf16_close(to_np(W[i]), refW, terms, what=f"W {i}")
+    for x, y in zip(runs[0][0] + runs[0][1], runs[1][0] + runs[1][1]):
+        assert torch.equal(x, y)
+
+
 def test_rownorm_overlap_matches_serial():
     """Wide-row kernels on the library's second stream give the same bits as running serially."""
     shapes = [(1536, 1536), (1536, 6144), (4608, 1536), (6144, 1536), (300, 1000), (1000, 300)]
