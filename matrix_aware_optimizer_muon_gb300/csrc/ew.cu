@@ -256,8 +256,13 @@ ew_tile_kernel(const __grid_constant__ EwParams p) {
         if (c >= cols) continue;
         XT* dst = X + (size_t)c * ld + rr;
         if (rr + 1 < rows) {
-          dst[0] = tb[cl][2 * lane];
-          dst[1] = tb[cl][2 * lane + 1];
+          if constexpr (sizeof(XT) == 2) {
+            // rr is even and ld a multiple of 8: one 4-byte store of the pair
+            *reinterpret_cast<__nv_bfloat162*>(dst) = *reinterpret_cast<const __nv_bfloat162*>(&tb[cl][2 * lane]);
+          } else {
+            dst[0] = tb[cl][2 * lane];
+            dst[1] = tb[cl][2 * lane + 1];
+          }
         } else if (rr < rows) {
           dst[0] = tb[cl][2 * lane];
         }
