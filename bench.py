@@ -386,69 +386,82 @@ def run_ours(args, torch):
 
     # End to end through the public API with host buffers (pinned): every optimizer step
     # uploads its gradients and downloads its updated weights inside the timed region.
-    # Copies are pipelined with compute the way a training loop would run them: G is
-    # double-buffered on the device (the upload for step t+1 runs during step t), and
-    # W is staged on the device after each step so that its download overlaps the
-    # next step.
+    # Copies are pipelined with compute the way a training loop would run them: G has
+    # NG device buffers, so uploads run up to NG - 1 steps ahead (through a long refresh
+    # step too), and W is staged into one of NW device buffers after each step, so that
+    # its download overlaps the following steps.
+    e2e_bufs = None
     if not args.no_e2e:
+        free = torch.cuda.mem_get_info(device)[0]
+        for ng, nw in ((3, 2), (2, 1)):   # fewer staging buffers when device memory is short
+            if (ng - 1) * tot * gb + nw * tot * wb + (1 << 30) <= free:
+                e2e_bufs = (ng, nw)
+                break
+        if e2e_bufs is None:
+            line["e2e"] = {"value": None, "unit": "ms", "skipped": "not enough device memory for the staging buffers"}
+    if e2e_bufs is not None:
+        NG, NW = e2e_bufs
         G_host = torch.empty(tot, dtype=gdt, pin_memory=True)
         W_host = torch.empty(tot, dtype=wdt, pin_memory=True)
         G_host.copy_(G_flat)
-        G2_flat = torch.empty_like(G_flat)
-        W_stage = torch.empty_like(W_flat)
-        G_bufs = [G_flat, G2_flat]
+        G_bufs = [G_flat] + [torch.empty_like(G_flat) for _ in range(NG - 1)]
+        W_stage = [torch.empty_like(W_flat) for _ in range(NW)]
         G_views = [[gb[o:o + a * b].view(a, b) for o, (a, b) in zip(offs, shapes)] for gb in G_bufs]
         comp = torch.cuda.current_stream()
         up, down = torch.cuda.Stream(), torch.cuda.Stream()
         torch.cuda.synchronize()
         n_e2e = max(1, min(args.steps, 5)) * wl.K
-        uploaded = [torch.cuda.Event() for _ in range(2)]
-        consumed = [torch.cuda.Event() for _ in range(2)]
-        staged = torch.cuda.Event()
-        downloaded = torch.cuda.Event()
+        uploaded = [torch.cuda.Event() for _ in range(NG)]
+        consumed = [torch.cuda.Event() for _ in range(NG)]
+        staged = [torch.cuda.Event() for _ in range(NW)]
+        downloaded = [torch.cuda.Event() for _ in range(NW)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def upload(j):   # step j's gradients into buffer j % NG, once step j - NG has used it
+            with torch.cuda.stream(up):
+                if j >= NG:
+                    up.wait_event(consumed[j % NG])
+                G_bufs[j % NG].copy_(G_host, non_blocking=True)
+                uploaded[j % NG].record(up)
+
         barrier(dist)
         e0.record(comp)
-        with torch.cuda.stream(up):
-            up.wait_event(e0)
-            G_bufs[0].copy_(G_host, non_blocking=True)
-            uploaded[0].record(up)
-        downloaded.record(comp)
+        up.wait_event(e0)
+        down.wait_event(e0)
+        for j in range(min(NG - 1, n_e2e)):
+            upload(j)
         for i in range(n_e2e):
-            cur = i & 1
-            if i + 1 < n_e2e:                     # upload the next step's gradients now
-                with torch.cuda.stream(up):
-                    if i >= 1:
-                        up.wait_event(consumed[1 - cur])
-                    G_bufs[1 - cur].copy_(G_host, non_blocking=True)
-                    uploaded[1 - cur].record(up)
-            comp.wait_event(uploaded[cur])
-            mm.muon_periodic_step(W, G_views[cur], M, step_counter[0], ws, K=wl.K, gamma=wl.gamma, mu=wl.mu,
+            if i + NG - 1 < n_e2e:
+                upload(i + NG - 1)
+            comp.wait_event(uploaded[i % NG])
+            mm.muon_periodic_step(W, G_views[i % NG], M, step_counter[0], ws, K=wl.K, gamma=wl.gamma, mu=wl.mu,
                                   eta=wl.eta, lam=wl.lam, ns5_mode=mode)
             step_counter[0] += 1
-            consumed[cur].record(comp)
-            comp.wait_event(downloaded)           # the previous download has left the stage
-            W_stage.copy_(W_flat, non_blocking=True)
-            staged.record(comp)
+            consumed[i % NG].record(comp)
+            k = i % NW
+            if i >= NW:
+                comp.wait_event(downloaded[k])   # stage buffer k is free once step i - NW's download is done
+            W_stage[k].copy_(W_flat, non_blocking=True)
+            staged[k].record(comp)
             with torch.cuda.stream(down):
-                down.wait_event(staged)
-                W_host.copy_(W_stage, non_blocking=True)
-                downloaded.record(down)
-        comp.wait_event(downloaded)
+                down.wait_event(staged[k])
+                W_host.copy_(W_stage[k], non_blocking=True)
+                downloaded[k].record(down)
+        comp.wait_stream(down)
         e1.record(comp)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / n_e2e, device)
         # The same copies with no compute between them: the floor the host link sets.
         l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         l0.record(comp)
-        for s_, dst, src in ((up, G_bufs, G_host), (down, None, W_stage)):
+        for s_, is_up in ((up, True), (down, False)):
             with torch.cuda.stream(s_):
                 s_.wait_event(l0)
                 for i in range(n_e2e):
-                    if dst is None:
-                        W_host.copy_(src, non_blocking=True)
+                    if is_up:
+                        G_bufs[i % NG].copy_(G_host, non_blocking=True)
                     else:
-                        dst[i & 1].copy_(src, non_blocking=True)
+                        W_host.copy_(W_stage[i % NW], non_blocking=True)
             comp.wait_stream(s_)
         l1.record(comp)
         torch.cuda.synchronize()
@@ -458,7 +471,7 @@ def run_ours(args, torch):
                        "copies_alone_ms": round(link_ms, 4),
                        "copies_alone_gbs": round((tot * gb + tot * wb) / link_ms / 1e6, 1),
                        "note": "G uploaded and W downloaded every step from/to pinned host memory, "
-                               "pipelined with compute (double-buffered G, W staged on the device); "
+                               f"pipelined with compute ({NG} device buffers for G, {NW} for staging W); "
                                "copies_alone_ms: the same copies with no compute"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
