@@ -12,7 +12,7 @@
 
 namespace muon {
 
-constexpr int SB = 64, SK = 16;
+constexpr int SB = 64, SK = 32;
 
 __global__ void __launch_bounds__(256) ns_simt_kernel(const __grid_constant__ NsParams p) {
   __shared__ float As[SK][SB + 4];
@@ -62,26 +62,41 @@ __global__ void __launch_bounds__(256) ns_simt_kernel(const __grid_constant__ Ns
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 
-  for (int k0 = 0; k0 < K; k0 += SK) {
-    for (int e = tid; e < SB * SK; e += 256) {
-      const int i = e / SK, k = e - (e / SK) * SK;
-      const int row = row0 + i;
-      As[k][i] = (row < n && k0 + k < K) ? A[(size_t)row * lda + k0 + k] : 0.f;
-    }
-    if (kind == GEMM_UPDATE) {
-      for (int e = tid; e < SB * SK; e += 256) {
+  // Operand slices of SK columns of K: the next slice is loaded into registers while
+  // the current one is multiplied out of shared memory (one barrier pair per slice).
+  constexpr int PER = SB * SK / 256;   // elements of each operand per thread and slice
+  float ra[PER], rb[PER];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int e = tid + q * 256;
+      {
+        const int i = e / SK, k = e - (e / SK) * SK;
+        const int row = row0 + i;
+        ra[q] = (row < n && k0 + k < K) ? A[(size_t)row * lda + k0 + k] : 0.f;
+      }
+      if (kind == GEMM_UPDATE) {
         const int k = e / SB, j = e - (e / SB) * SB;
         const int col = col0 + j;
-        Bs[k][j] = (k0 + k < K && col < ncols) ? B[(size_t)(k0 + k) * ldb + col] : 0.f;
-      }
-    } else {
-      for (int e = tid; e < SB * SK; e += 256) {
+        rb[q] = (k0 + k < K && col < ncols) ? B[(size_t)(k0 + k) * ldb + col] : 0.f;
+      } else {
         const int j = e / SK, k = e - (e / SK) * SK;
         const int col = col0 + j;
-        Bs[k][j] = (col < ncols && k0 + k < K) ? B[(size_t)col * ldb + k0 + k] : 0.f;
+        rb[q] = (col < ncols && k0 + k < K) ? B[(size_t)col * ldb + k0 + k] : 0.f;
       }
     }
+  };
+  load(0);
+  for (int k0 = 0; k0 < K; k0 += SK) {
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int e = tid + q * 256;
+      As[e - (e / SK) * SK][e / SK] = ra[q];
+      if (kind == GEMM_UPDATE) Bs[e / SB][e - (e / SB) * SB] = rb[q];
+      else Bs[e - (e / SK) * SK][e / SK] = rb[q];
+    }
     __syncthreads();
+    if (k0 + SK < K) load(k0 + SK);   // in flight during the products below
 #pragma unroll
     for (int k = 0; k < SK; ++k) {
       float a[4], b[4];
