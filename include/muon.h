@@ -150,13 +150,14 @@ int muon_apply(const muon_matrix* mats, int n, const void* const* U, int u_dtype
  *   M <- mu*M + G;
  *   U = NS5(M) (refresh) or RowNorm(M) (otherwise);
  *   W <- W - eta*(s*U + lambda*W), s = 0.2*sqrt(max(A, B)), times gamma when not refreshing.
- * On refresh steps the apply is fused into the last Newton-Schulz GEMM; on
- * RowNorm steps momentum, normalisation and apply are one pass over memory
- * (tall matrices whose strips do not fit the cluster kernel take two passes).
- * The wide-row kernels of a RowNorm step run on a second stream owned by the
- * library (one per host thread and device), forked from and joined back to
- * `stream` with events, so the call stays ordered on `stream` and capturable.  branch_out (host, optional)
- * receives MUON_BRANCH_NS5 or MUON_BRANCH_ROWNORM. */
+ * On refresh steps the apply is fused into the last Newton-Schulz GEMM.  On
+ * RowNorm steps, wide and square matrices take one pass over memory (momentum,
+ * row norms and apply); tall matrices take two row-contiguous passes in one
+ * launch, the second re-reading the new momentum from L2.  The wide-row kernels
+ * of a RowNorm step run on a second stream owned by the library (one per host
+ * thread and device), forked from and joined back to `stream` with events, so
+ * the call stays ordered on `stream` and capturable.  branch_out (host,
+ * optional) receives MUON_BRANCH_NS5 or MUON_BRANCH_ROWNORM. */
 int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, float gamma,
                        float mu, float eta, float lambda, int ns5_mode, void* ws,
                        size_t ws_bytes, muon_stream_t stream, int* branch_out);

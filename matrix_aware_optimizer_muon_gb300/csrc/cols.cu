@@ -1,6 +1,8 @@
 // Single-pass RowNorm step for tall matrices (A > B), whose RowNorm lines are
 // the B columns ("Scaling Muon for Diffusion Transformers", distributed-
 // implementation paragraph: tall matrices reduce per-column norm scalars).
+// Selected by MUON_DEBUG_TALL_CLUSTER; the default tall path is tall.cu, whose
+// row-contiguous passes reach higher DRAM efficiency than these 32-column strips.
 //
 // A thread-block cluster of CL CTAs owns one strip of CW columns of one matrix;
 // CTA k of the cluster owns rows [k*slab, (k+1)*slab).  Each CTA streams its slab
