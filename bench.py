@@ -245,7 +245,7 @@ def run_reference(args, torch):
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": wl.key, "matrices": len(wl.matrices), "params": wl.n_params, "K": wl.K,
-                       "gamma": wl.gamma, "parallelism": "replicas"},
+                       "gamma": wl.gamma, "parallelism": "replicas" if args.gpus > 1 else "single process"},
             "cpu_baseline": {"value": round(value, 3), "unit": "ms", "cores": cores, "kind": "oracle",
                              "sample": sample, "detail": detail},
             "e2e": {"value": round(value, 3), "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
