@@ -23,9 +23,11 @@
  *  - Memory: all tensor pointers are DEVICE pointers owned by the caller (for
  *    example PyTorch allocations).  The library allocates no device memory and
  *    frees nothing.  Scratch space comes from the caller's workspace `ws`
- *    (device, 256-byte aligned, at least muon_workspace_size() bytes).  Arrays of
- *    muon_matrix and arrays of output pointers are HOST arrays, read during the
- *    call only.
+ *    (device, 256-byte aligned, at least muon_workspace_size() bytes).  A
+ *    workspace holds one call's scratch: two calls whose GPU work may overlap
+ *    (different streams, no ordering between them) need two workspaces.  Arrays
+ *    of muon_matrix and arrays of output pointers are HOST arrays, read during
+ *    the call only.
  *  - Layout: W, G, M, O and R are row-major A x B with leading dimension B (dense).
  *    M is always fp32.  W and G are fp32 or bf16 (MUON_DTYPE_*); within one call
  *    every matrix uses the same (w_dtype, g_dtype) pair.
