@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph per-branch timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--K", type=int, default=0,
                     help="override the schedule period K (1 = vanilla Muon: every step is a refresh)")
@@ -424,6 +425,53 @@ def run_ours(args, torch):
     # NG device buffers, so uploads run up to NG - 1 steps ahead (through a long refresh
     # step too), and W is staged into one of NW device buffers after each step, so that
     # its download overlaps the following steps.
+    # Per-branch timing as CUDA-graph replays: one refresh step and one RowNorm step are
+    # each captured once and replayed 20 times (the median of the per-replay event
+    # times is reported).  Replays repeat the same step on the same buffers, which is
+    # what a timing of the step needs; the schedule itself was exercised above.
+    if not args.no_graph:
+        try:
+            gstream = torch.cuda.Stream()
+            gstream.wait_stream(torch.cuda.current_stream())
+            graphs = {}
+            branches = [("refresh", 0)] + ([("rownorm", 1)] if wl.K > 1 else [])
+            with torch.cuda.stream(gstream):
+                for name, st in branches:   # warm the exact call once on this stream
+                    mm.muon_periodic_step(W, G, M, st, ws, K=wl.K, gamma=wl.gamma, mu=wl.mu, eta=wl.eta,
+                                          lam=wl.lam, ns5_mode=mode)
+            torch.cuda.synchronize()
+            for name, st in branches:
+                g_ = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g_, stream=gstream):
+                    mm.muon_periodic_step(W, G, M, st, ws, K=wl.K, gamma=wl.gamma, mu=wl.mu, eta=wl.eta,
+                                          lam=wl.lam, ns5_mode=mode)
+                graphs[name] = g_
+            torch.cuda.synchronize()
+            gres = {}
+            for name, g_ in graphs.items():
+                g_.replay()
+                torch.cuda.synchronize()
+                ts = []
+                for _ in range(20):
+                    if flush:
+                        scratch.fill_(0.0)
+                    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a_.record()
+                    g_.replay()
+                    b_.record()
+                    torch.cuda.synchronize()
+                    ts.append(a_.elapsed_time(b_))
+                gres[name + "_ms_median"] = round(statistics.median(ts), 4)
+            if mm.muon_check_status(ws) != mm.MUON_OK:
+                raise RuntimeError("device status error in the graph replays")
+            if wl.K > 1:
+                gres["k_average_ms"] = round((gres["refresh_ms_median"] + (wl.K - 1) * gres["rownorm_ms_median"])
+                                             / wl.K, 4)
+            gres["replays"] = 20
+            line["graph"] = gres
+        except RuntimeError as exc:   # capture unsupported here: leave the field out, say why
+            line["graph"] = {"skipped": str(exc)[:200]}
+
     e2e_bufs = None
     if not args.no_e2e:
         free = torch.cuda.mem_get_info(device)[0]
