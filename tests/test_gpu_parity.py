@@ -127,9 +127,12 @@ def test_apply_parity(wdt, udt):
 TALL_PATHS = {"l2pass": 0, "cluster": mm.MUON_DEBUG_TALL_CLUSTER, "two_pass": mm.MUON_DEBUG_NO_CLUSTER}
 
 
-@pytest.mark.parametrize("path", list(TALL_PATHS))
-@pytest.mark.parametrize("dt", ["bf16", "f32"])
-def test_rownorm_step_parity(dt, path):
+ROWNORM_CASES = [(dt, dt, path) for path in TALL_PATHS for dt in ("bf16", "f32")] + \
+    [("bf16", "f32", "l2pass"), ("f32", "bf16", "l2pass")]
+
+
+@pytest.mark.parametrize("wdt,gdt,path", ROWNORM_CASES)
+def test_rownorm_step_parity(wdt, gdt, path):
     """Wide rows (single pass) and tall columns on each tall route, ragged and degenerate
     shapes.  For the L2 two-pass kernel: (4608, 1536) has 12 column blocks x 36 row blocks
     (more chunks than the pass-2 lag), the two (1000, 300) share one launch with a ragged
@@ -138,11 +141,11 @@ def test_rownorm_step_parity(dt, path):
     memory.  (13, 7) and (517, 1) have B % 4 != 0 and take the plain two-pass kernels."""
     shapes = [(256, 1024), (300, 1000), (1000, 300), (1536, 1536), (7, 13), (13, 7), (1, 517), (517, 1),
               (3, 20000), (129, 129), (4608, 1536), (300, 36), (40000, 8), (70000, 8), (33, 4), (1000, 300)]
-    W0, Gs = inputs(shapes, dt, dt, 2)
+    W0, Gs = inputs(shapes, wdt, gdt, 2)
     M0 = rand_M(shapes, seed=8, zero_line=True)
-    W = [to_dev(w, dt) for w in W0]
+    W = [to_dev(w, wdt) for w in W0]
     M = [to_dev(m, "f32") for m in M0]
-    G = [to_dev(g, dt) for g in Gs[1]]
+    G = [to_dev(g, gdt) for g in Gs[1]]
     ws = mm.alloc_workspace(shapes)
     mm.muon_debug_set(TALL_PATHS[path], 0)
     try:
@@ -155,7 +158,7 @@ def test_rownorm_step_parity(dt, path):
         refW, refM, refresh = muon_ref.periodic_step(W0[i], M0[i], Gs[1][i], 1, 3, 0.15, 0.95, 0.02, 0.01)
         assert not refresh
         assert_f32_close(to_np(M[i]), refM, what=f"M {shapes[i]}")
-        if dt == "f32":
+        if wdt == "f32":
             assert_f32_close(to_np(W[i]), refW, what=f"W {shapes[i]}")
         else:
             a, b = shapes[i]
