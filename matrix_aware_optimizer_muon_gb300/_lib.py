@@ -14,7 +14,9 @@ from typing import List, Optional, Sequence
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libmuon_gb300.so")
+# The in-tree build; MUON_GB300_LIB names another build of the same sources (for
+# example one compiled with tuning defines through build.build(defines=..., out=...)).
+LIB_PATH = os.environ.get("MUON_GB300_LIB") or os.path.join(HERE, "libmuon_gb300.so")
 
 MUON_OK = 0
 MUON_ERR_INVALID = -1
