@@ -200,11 +200,14 @@ def test_ns5_parity(mode, tol, steps):
         err = rel_fro(to_np(O[i]), ref)
         worst[shapes[i]] = err
         assert err <= tol, (shapes[i], err)
-        # the bf16 path keeps a*X in higher precision in the early iterations; on
-        # matrices spanning several tiles that holds its error near 4e-3
-        # (degenerate 1 x n, n x 1 and 8 x 8 inputs sit near 1.4e-2)
+        # the bf16 path keeps a*X in higher precision in the early iterations (fp32 M,
+        # then the bf16 residual of X); on matrices spanning several tiles that holds
+        # its error at 4e-3 to 6.5e-3 measured (a CPU emulation of the same rounding
+        # points predicts 3.4e-3 to 4.7e-3 before O's own bf16 rounding); without the
+        # residual it would be 1e-2 to 2e-2.  Degenerate 1 x n, n x 1 and 8 x 8
+        # inputs sit near 1.1e-2 to 1.7e-2.
         if mode == "bf16" and min(shapes[i]) >= 128:
-            assert err <= 1e-2, (shapes[i], err)
+            assert err <= 8e-3, (shapes[i], err)
         assert np.array_equal(to_np(M[i]), M0[i].astype(np.float64))
     print(f"ns5 {mode} steps={steps}: " + ", ".join(f"{k[0]}x{k[1]} {v:.2e}" for k, v in worst.items()))
 
