@@ -57,12 +57,20 @@ class PeriodicMuon:
                               ns5_mode=self.ns5_mode)}
 
     def load_state_dict(self, sd: Dict) -> None:
+        """Restores the momentum, the AdamW moments and the step.  The schedule period K
+        and the NS5 mode must match the saved ones (they change which branch a step takes
+        and its arithmetic); learning rate, weight decay and gamma may differ."""
+        hyper = sd.get("hyper", {})
+        for key in ("K", "ns5_mode"):
+            if key in hyper and hyper[key] != getattr(self, key):
+                raise ValueError(f"state was saved with {key}={hyper[key]!r}, this optimizer has {getattr(self, key)!r}")
         if len(sd["M"]) != len(self.M):
             raise ValueError("state has a different number of matrices")
-        for dst, src in zip(self.M, sd["M"]):
+        aux_m, aux_v = sd.get("aux_m", []), sd.get("aux_v", [])
+        if len(aux_m) != len(self.aux_m) or len(aux_v) != len(self.aux_v):
+            raise ValueError("state has a different number of auxiliary parameters")
+        for dst, src in zip(self.M + self.aux_m + self.aux_v, list(sd["M"]) + list(aux_m) + list(aux_v)):
             if tuple(dst.shape) != tuple(src.shape):
                 raise ValueError("state shape mismatch")
-            dst.copy_(src)
-        for dst, src in zip(self.aux_m + self.aux_v, sd.get("aux_m", []) + sd.get("aux_v", [])):
             dst.copy_(src)
         self.step_count = int(sd["step"])

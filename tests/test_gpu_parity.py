@@ -623,6 +623,41 @@ def test_adamw_parity(pdt, gdt):
             refP[i] = muon_ref.round_to_storage(refP[i], pdt)
 
 
+def test_periodic_muon_checkpoint_resumes_bit_exact():
+    """A wrapper checkpoint (momentum, AdamW moments, step) taken after 2 steps and loaded
+    into a fresh optimizer continues exactly like the uninterrupted run; a checkpoint
+    from a different K is refused."""
+    shapes = [(256, 512), (512, 256)]
+    W0, Gs = inputs(shapes, "bf16", "bf16", 5)
+    aux0 = [np.linspace(-1, 1, 300, dtype=np.float32), np.linspace(0.5, 2, 77, dtype=np.float32)]
+    aux_g = [[np.sin(np.arange(a.size) * (t + 1)).astype(np.float32) * 1e-2 for a in aux0] for t in range(5)]
+
+    def make():
+        W = [to_dev(w, "bf16") for w in W0]
+        A = [torch.from_numpy(a.copy()).to(dev()) for a in aux0]
+        return W, A, mm.PeriodicMuon(W, aux_params=A)
+
+    Wa, Aa, opt_a = make()
+    for t in range(5):
+        opt_a.step([to_dev(g, "bf16") for g in Gs[t]], [torch.from_numpy(g).to(dev()) for g in aux_g[t]])
+    Wb, Ab, opt_b = make()
+    for t in range(2):
+        opt_b.step([to_dev(g, "bf16") for g in Gs[t]], [torch.from_numpy(g).to(dev()) for g in aux_g[t]])
+    torch.cuda.synchronize()
+    sd = {k: ([x.cpu() for x in v] if isinstance(v, list) else v) for k, v in opt_b.state_dict().items()}
+    Wc = [w.clone() for w in Wb]
+    Ac = [a.clone() for a in Ab]
+    opt_c = mm.PeriodicMuon(Wc, aux_params=Ac)
+    opt_c.load_state_dict(sd)
+    for t in range(2, 5):
+        opt_c.step([to_dev(g, "bf16") for g in Gs[t]], [torch.from_numpy(g).to(dev()) for g in aux_g[t]])
+    torch.cuda.synchronize()
+    for x, y in zip(Wa + Aa + opt_a.M, Wc + Ac + opt_c.M):
+        assert torch.equal(x, y)
+    with pytest.raises(ValueError):
+        mm.PeriodicMuon([w.clone() for w in Wb], K=4, aux_params=[a.clone() for a in Ab]).load_state_dict(sd)
+
+
 def test_periodic_muon_wrapper_matches_direct_calls():
     """The stateful wrapper (momentum buffers, workspace, step counter, auxiliary AdamW)
     gives the same bits as calling the entry points directly."""
