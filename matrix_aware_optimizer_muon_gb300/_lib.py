@@ -279,6 +279,17 @@ def muon_periodic_step(W: Sequence[torch.Tensor], G: Sequence[torch.Tensor], M: 
     return br.value
 
 
+def periodic_step_prepared(arr, n: int, step: int, ws: torch.Tensor, K: int, gamma: float, mu: float, eta: float,
+                           lam: float, ns5_mode: str, stream=None) -> int:
+    """muon_periodic_step on a matrix array built once by make_matrices and kept by the
+    caller (the stateful wrapper updates only the gradient pointers between steps)."""
+    br = ctypes.c_int(-1)
+    st = load_library().muon_periodic_step(arr, n, int(step), int(K), gamma, mu, eta, lam, _NS5_MODES[ns5_mode],
+                                           _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(br))
+    _check("muon_periodic_step", st)
+    return br.value
+
+
 def muon_debug_set(flags: int = 0, timeout_ms: int = 0):
     _check("muon_debug_set", load_library().muon_debug_set(int(flags), int(timeout_ms)))
 

@@ -33,11 +33,21 @@ class PeriodicMuon:
         self.M = [torch.zeros(p.shape, dtype=torch.float32, device=dev) for p in self.params]
         self.ws = _lib.alloc_workspace([tuple(p.shape) for p in self.params], ns5_mode, device=dev)
         self.step_count = 0
+        # W and M never move, so the C matrix array is built once; each step only
+        # points it at that step's gradients (after checking them like the array build does).
+        self._arr, self._n = _lib.make_matrices(self.M, self.params, self.params)
+        self._gdt = None
 
     def step(self, grads: Sequence[torch.Tensor], aux_grads: Sequence[torch.Tensor] = (), stream=None) -> int:
-        br = _lib.muon_periodic_step(self.params, grads, self.M, self.step_count, self.ws, K=self.K,
-                                     gamma=self.gamma, mu=self.mu, eta=self.eta, lam=self.lam,
-                                     ns5_mode=self.ns5_mode, stream=stream)
+        if len(grads) != self._n:
+            raise ValueError("one gradient per matrix")
+        for i, (g, p) in enumerate(zip(grads, self.params)):
+            if g.shape != p.shape:
+                raise ValueError("W, G and M must have the same shape")
+            self._arr[i].G = _lib._ptr(g)
+            self._arr[i].g_dtype = _lib._dt(g)
+        br = _lib.periodic_step_prepared(self._arr, self._n, self.step_count, self.ws, self.K, self.gamma, self.mu,
+                                         self.eta, self.lam, self.ns5_mode, stream=stream)
         if self.aux:
             if len(aux_grads) != len(self.aux):
                 raise ValueError("one gradient per auxiliary parameter")
