@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph per-branch timing")
+    ap.add_argument("--scale-mode", default="adjusted_lr", choices=["adjusted_lr", "update_norm"],
+                    help="update scale: 0.2*sqrt(max(A,B)) (Eq. 7, default) or 0.2/RMS(U) (Eq. 6)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--K", type=int, default=0,
                     help="override the schedule period K (1 = vanilla Muon: every step is a refresh)")
@@ -294,7 +296,7 @@ def run_ours(args, torch):
 
     def opt_step(step):
         mm.muon_periodic_step(W, G, M, step, ws, K=wl.K, gamma=wl.gamma, mu=wl.mu, eta=wl.eta, lam=wl.lam,
-                              ns5_mode=mode)
+                              ns5_mode=mode, scale_mode=args.scale_mode)
         launches[0] += mm.muon_launch_count()
 
     step_counter = [0]
@@ -382,6 +384,7 @@ def run_ours(args, torch):
         "data": "synthetic",
         "config": {"workload": wl.key, "matrices": len(shapes), "params": wl.n_params,
                    "K": wl.K, "gamma": wl.gamma, "mu": wl.mu, "eta": wl.eta, "lambda": wl.lam,
+                   "scale_mode": args.scale_mode,
                    "step": (f"one K={wl.K} period: 1 NS5 refresh + {wl.K - 1} RowNorm optimizer steps; value = period/{wl.K}"
                             if wl.K > 1 else "vanilla Muon (K=1): every optimizer step is an NS5 refresh"),
                    "l2": (f"inputs larger than L2 (W+G+M {in_bytes / 1e9:.1f} GB vs 129 MB L2), no flush" if not flush
@@ -438,13 +441,13 @@ def run_ours(args, torch):
             with torch.cuda.stream(gstream):
                 for name, st in branches:   # warm the exact call once on this stream
                     mm.muon_periodic_step(W, G, M, st, ws, K=wl.K, gamma=wl.gamma, mu=wl.mu, eta=wl.eta,
-                                          lam=wl.lam, ns5_mode=mode)
+                                          lam=wl.lam, ns5_mode=mode, scale_mode=args.scale_mode)
             torch.cuda.synchronize()
             for name, st in branches:
                 g_ = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g_, stream=gstream):
                     mm.muon_periodic_step(W, G, M, st, ws, K=wl.K, gamma=wl.gamma, mu=wl.mu, eta=wl.eta,
-                                          lam=wl.lam, ns5_mode=mode)
+                                          lam=wl.lam, ns5_mode=mode, scale_mode=args.scale_mode)
                 graphs[name] = g_
             torch.cuda.synchronize()
             gres = {}
@@ -517,7 +520,7 @@ def run_ours(args, torch):
                 upload(i + NG - 1)
             comp.wait_event(uploaded[i % NG])
             mm.muon_periodic_step(W, G_views[i % NG], M, step_counter[0], ws, K=wl.K, gamma=wl.gamma, mu=wl.mu,
-                                  eta=wl.eta, lam=wl.lam, ns5_mode=mode)
+                                  eta=wl.eta, lam=wl.lam, ns5_mode=mode, scale_mode=args.scale_mode)
             step_counter[0] += 1
             consumed[i % NG].record(comp)
             k = i % NW

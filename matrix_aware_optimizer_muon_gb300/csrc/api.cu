@@ -847,6 +847,7 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
             e.tiles_c = cdiv(g.m, APPLYWS_TILE);
             e.tile_begin = tiles;
             e.scale_index = k;
+            e.vec = aligned(mats[k].W, 16) && (mp.tall ? g.n % 8 == 0 : g.m % 8 == 0);
             tiles += cdiv(g.n, APPLYWS_TILE) * e.tiles_c;
           }
           ap.nmat = j;

@@ -510,6 +510,21 @@ __global__ void nz_rms_kernel(const __grid_constant__ NzRmsParams p) {
   p.rms_out[o] = p.numel[i] > 0 ? (float)sqrt((double)p.nz[o] / p.numel[i]) : 0.f;
 }
 
+// 8 consecutive bf16 values <-> float[8]; the pointer is 16-byte aligned
+__device__ __forceinline__ void load_bf16x8(const bf16* p, float v[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    v[2 * h] = __uint_as_float(w[h] << 16);
+    v[2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void store_bf16x8(bf16* p, const float v[8]) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
 // W <- W - eta*(scale*O + lambda*W) for O kept in the workspace on the short side
 // (n x m, leading dimension ld).  64 x 64 tiles of O pass through shared memory so
 // that a tall W (m x n, W[c][r] = update of O[r][c]) is read and written along its
@@ -548,7 +563,39 @@ apply_ws_kernel(const __grid_constant__ ApplyWsParams p) {
   const OT* O = reinterpret_cast<const OT*>(mt.O);
   const bf16* L = reinterpret_cast<const bf16*>(mt.O_lo);
   constexpr int PER = APPLYWS_TILE * APPLYWS_TILE / 256;   // elements per thread (256 threads)
-  {
+  constexpr bool kBf16 = sizeof(WT) == 2 && sizeof(OT) == 2;
+  if constexpr (kBf16) {
+    // O (and its residual) as 8-element vectors: lane v takes row v / 8 of the tile,
+    // columns (v % 8) * 8 .. + 7 (rows of O are 16-byte aligned: ld is a multiple of 8)
+    float f[PER / 8][8];
+#pragma unroll
+    for (int q = 0; q < PER / 8; ++q) {
+      const int v = threadIdx.x + q * 256;
+      const int r = r0 + (v >> 3), c = c0 + (v & 7) * 8;
+      const size_t off = (size_t)r * mt.ld + c;
+      if (r < n && c + 8 <= m) {
+        float lo[8];
+        load_bf16x8(O + off, f[q]);
+        if (L) {
+          load_bf16x8(L + off, lo);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[q][k] += lo[k];
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          f[q][k] = 0.f;
+          if (r < n && c + k < m) f[q][k] = to_f32(O[off + k]) + (L ? __bfloat162float(L[off + k]) : 0.f);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < PER / 8; ++q) {
+      const int v = threadIdx.x + q * 256;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t[v >> 3][(v & 7) * 8 + k] = f[q][k];
+    }
+  } else {
     float ov[PER];
 #pragma unroll
     for (int q = 0; q < PER; ++q) {
@@ -570,6 +617,55 @@ apply_ws_kernel(const __grid_constant__ ApplyWsParams p) {
   __syncthreads();
   const float sc = p.scale[mt.scale_index];
   WT* W = reinterpret_cast<WT*>(mt.W);
+  if constexpr (kBf16) {
+    if (mt.vec) {
+      // W in its own orientation as 8-element row segments: lane v takes W row v / 8 of
+      // the tile and W columns (v % 8) * 8 .. + 7 (a wide W row is an O row; a tall W
+      // row is an O column, read from the tile transposed)
+      float wv[PER / 8][8];
+      bool ok[PER / 8];
+      size_t widx[PER / 8];
+#pragma unroll
+      for (int q = 0; q < PER / 8; ++q) {
+        const int v = threadIdx.x + q * 256;
+        const int a = v >> 3, e = (v & 7) * 8;
+        if (!mt.tall) {
+          ok[q] = r0 + a < n && c0 + e + 8 <= m;
+          widx[q] = (size_t)(r0 + a) * m + (c0 + e);
+        } else {
+          ok[q] = c0 + a < m && r0 + e + 8 <= n;
+          widx[q] = (size_t)(c0 + a) * n + (r0 + e);
+        }
+        if (ok[q]) load_bf16x8(W + widx[q], wv[q]);
+      }
+#pragma unroll
+      for (int q = 0; q < PER / 8; ++q) {
+        const int v = threadIdx.x + q * 256;
+        const int a = v >> 3, e = (v & 7) * 8;
+        if (ok[q]) {
+          float o[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float u = mt.tall ? t[e + k][a] : t[a][e + k];
+            o[k] = wv[q][k] - p.eta * (sc * u + p.lam * wv[q][k]);
+          }
+          store_bf16x8(W + widx[q], o);
+        } else {
+          // ragged edge of the matrix: element by element
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = mt.tall ? e + k : a, cc = mt.tall ? a : e + k;
+            if (r0 + rr < n && c0 + cc < m) {
+              const size_t wi = mt.tall ? (size_t)(c0 + cc) * n + (r0 + rr) : (size_t)(r0 + rr) * m + (c0 + cc);
+              const float w = ld1(W + wi);
+              st1(W + wi, w - p.eta * (sc * t[rr][cc] + p.lam * w));
+            }
+          }
+        }
+      }
+      return;
+    }
+  }
   // every element's W load is issued before the first store (one DRAM round trip)
   float wv[PER];
 #pragma unroll

@@ -210,6 +210,7 @@ struct ApplyWsMat {
   int tiles_c;                // ceil(m / 64)
   int tile_begin;
   int scale_index;
+  int vec;                    // W 16-byte aligned with rows a multiple of 8 elements: 16-byte accesses
 };
 struct ApplyWsParams {
   ApplyWsMat mat[APPLYWS_MAX_MATS];
