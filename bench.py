@@ -34,7 +34,7 @@ L2_BYTES = 129e6
 # set (the same shape mix, 1/8 of the matrices) scaled by 8; see
 # profiles/ns_tc_kernel_traffic_mmdit-1.3b.md.  Valid only for the kernel sources
 # it was measured on (hash below); otherwise the roofline reports null.
-NS5_TRAFFIC = {"mmdit-1.3b": {"bytes_per_launch": 4.70e9, "sources": "cd9f8ea245ff1f16"}}
+NS5_TRAFFIC = {"mmdit-1.3b": {"bytes_per_launch": 4.70e9, "sources": "a88d3f837d9e80c0"}}
 NS5_SOURCES = ["ns_tc.cu", "ns_common.cuh", "ptx.cuh", "common.cuh", "internal.h", "api.cu"]
 
 
