@@ -840,15 +840,25 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
             e.W = mats[k].W;
             e.O = w + g.x1 + moff * esize;                       // output of the last UPDATE
             e.O_lo = tc ? (const void*)(w + g.lo0 + moff * 2) : nullptr;
-            e.n = g.n;
-            e.m = g.m;
-            e.ld = g.ld_m;
-            e.tall = mp.tall;
-            e.tiles_c = cdiv(g.m, APPLYWS_TILE);
+            if (tc && mp.tall) {
+              // the tensor-core path wrote a tall matrix's O in W's orientation
+              // (m x n, leading dimension n): an elementwise pass over W
+              e.n = g.m;
+              e.m = g.n;
+              e.ld = g.n;
+              e.tall = 0;
+            } else {
+              e.n = g.n;
+              e.m = g.m;
+              e.ld = g.ld_m;
+              e.tall = mp.tall;
+            }
+            e.tiles_c = cdiv(e.m, APPLYWS_TILE);
             e.tile_begin = tiles;
             e.scale_index = k;
-            e.vec = aligned(mats[k].W, 16) && (mp.tall ? g.n % 8 == 0 : g.m % 8 == 0);
-            tiles += cdiv(g.n, APPLYWS_TILE) * e.tiles_c;
+            e.vec = aligned(mats[k].W, 16) && (e.tall ? e.n % 8 == 0 : e.m % 8 == 0);
+            e.ovec = e.ld % 8 == 0;
+            tiles += cdiv(e.n, APPLYWS_TILE) * e.tiles_c;
           }
           ap.nmat = j;
           ap.total_tiles = tiles;

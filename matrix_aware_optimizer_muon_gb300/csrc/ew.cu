@@ -573,7 +573,7 @@ apply_ws_kernel(const __grid_constant__ ApplyWsParams p) {
       const int v = threadIdx.x + q * 256;
       const int r = r0 + (v >> 3), c = c0 + (v & 7) * 8;
       const size_t off = (size_t)r * mt.ld + c;
-      if (r < n && c + 8 <= m) {
+      if (mt.ovec && r < n && c + 8 <= m) {
         float lo[8];
         load_bf16x8(O + off, f[q]);
         if (L) {

@@ -211,6 +211,7 @@ struct ApplyWsMat {
   int tile_begin;
   int scale_index;
   int vec;                    // W 16-byte aligned with rows a multiple of 8 elements: 16-byte accesses
+  int ovec;                   // O's rows start 16-byte aligned (ld a multiple of 8): 16-byte loads
 };
 struct ApplyWsParams {
   ApplyWsMat mat[APPLYWS_MAX_MATS];

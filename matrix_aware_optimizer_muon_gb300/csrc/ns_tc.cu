@@ -248,7 +248,21 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
 #pragma unroll
       for (int j = 0; j < 32; ++j) osq = (c0 + j < m) ? fmaf(v[j], v[j], osq) : osq;
     }
-    if (!p.last_iter || p.dst_mode == 2) {
+    if (p.last_iter && p.dst_mode == 2 && (p.flags[gm] & NS_TALL)) {
+      // O of a tall matrix kept for Eq. (6) in W's orientation (m x n, leading
+      // dimension n, in this matrix's slot of the output buffers): consecutive lanes
+      // write consecutive elements, and the apply pass needs no transpose
+      const size_t base = (size_t)ti.mat * G.stride_nm + r;
+      bf16* Ot = reinterpret_cast<bf16*>(G.out) + base;
+      bf16* Lt = G.lo_out ? reinterpret_cast<bf16*>(G.lo_out) + base : nullptr;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < m) {
+          const bf16 h = __float2bfloat16_rn(v[j]);
+          Ot[(size_t)(c0 + j) * n] = h;
+          if (Lt) Lt[(size_t)(c0 + j) * n] = __float2bfloat16_rn(v[j] - __bfloat162float(h));
+        }
+    } else if (!p.last_iter || p.dst_mode == 2) {
       const size_t off = (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m + c0;
       bf16* Xout = reinterpret_cast<bf16*>(G.out) + off;
       bf16* Lout = G.lo_out ? reinterpret_cast<bf16*>(G.lo_out) + off : nullptr;
