@@ -8,7 +8,9 @@
 //    RowNorm pass W <- W - eta*(s*M/||line|| + lambda*W) (Eq. (4) with the
 //    Periodic Row-wise scale).
 //  * rows_kernel: the whole RowNorm step for a wide/square matrix in one pass:
-//    one CTA per row keeps the row in registers (momentum, row norm, apply).
+//    one CTA per row keeps the row in registers (momentum, row norm, apply);
+//    rows_wide_kernel: the same for rows of 6145..10240 columns, shaped for two
+//    CTAs per SM.
 //  * apply_kernel: W <- W - eta*(s*U + lambda*W) from a given direction U.
 //  * fro_final_kernel / line_final_kernel: fixed-order reductions of partials.
 //
@@ -362,6 +364,111 @@ rows_kernel(const __grid_constant__ RowsParams p) {
       for (int j = 0; j < 4; ++j)
         if (c + j < cols) { Mp[c + j] = v[k][j]; st1(Wp + c + j, o[j]); }
     }
+  }
+}
+
+// Rows of 6145..10240 columns: 512 threads with 4-5 four-element chunks each, at
+// most 64 registers a thread (the 1024-thread bound), so two CTAs per SM and one
+// row's reduction and stores overlap another's loads.  The general kernel above
+// takes up to 864 threads here, one CTA per SM (measured 5.7 against 7.1 TB/s on
+// 2560 x 10240 matrices).  The element-load path is a kernel of its own
+// (kVec = false), so that its registers do not count against the vector path.
+//
+// RowNorm of one row with cols % 4 != 0 or unaligned bases: element loads.
+template <typename WT, typename GT, int CPT>
+__device__ __forceinline__ void rows_scalar(float* __restrict__ Mp, const GT* __restrict__ Gp, WT* __restrict__ Wp,
+                                         int cols, float scale, int* nz, float mu, float eta, float lam,
+                                         float* red) {
+  float v[CPT][4], w[CPT][4];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) {
+    const int c = (threadIdx.x + k * blockDim.x) * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool ok = c + j < cols;
+      v[k][j] = ok ? mu * Mp[c + j] + ld1(Gp + c + j) : 0.f;
+      w[k][j] = ok ? ld1(Wp + c + j) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ss = fmaf(v[k][j], v[k][j], ss);
+  }
+  const float inv = inv_norm_from_sumsq(block_sum(ss, red));
+  if (nz && threadIdx.x == 0 && inv > 0.f) atomicAdd(nz, 1);   // telemetry: nonzero rows
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) {
+    const int c = (threadIdx.x + k * blockDim.x) * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (c + j < cols) {
+        Mp[c + j] = v[k][j];
+        st1(Wp + c + j, w[k][j] - eta * (scale * (v[k][j] * inv) + lam * w[k][j]));
+      }
+  }
+}
+
+// kVec: every matrix of the launch has vec set (cols % 4 == 0, aligned bases).
+template <typename WT, typename GT, int CPT, bool kVec>
+__global__ void __launch_bounds__(1024)
+rows_wide_kernel(const __grid_constant__ RowsParams p) {
+  __shared__ float red[32];
+  const int rg = blockIdx.x;
+  const RowsMat& mt = p.mat[find_mat_rows(p, rg)];
+  const int r = rg - mt.row_begin;
+  const int cols = mt.cols;
+  const size_t base = (size_t)r * (size_t)cols;
+  float* __restrict__ Mp = mt.M + base;
+  const GT* __restrict__ Gp = reinterpret_cast<const GT*>(mt.G) + base;
+  WT* __restrict__ Wp = reinterpret_cast<WT*>(mt.W) + base;
+
+  float ss = 0.f;
+  if constexpr (kVec) {
+    // Every chunk's loads are issued before any is used: one DRAM round trip per
+    // row.  The raw registers start at zero and only the loads are conditional, so
+    // the conversions below run unconditionally and no load can be moved down to
+    // a use under the same bound (which serialises the round trips).
+    float v[CPT][4], w[CPT][4];
+    {
+      float4 mr[CPT] = {};
+      typename Raw4<GT>::type gr[CPT] = {};
+      typename Raw4<WT>::type wr[CPT] = {};
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) {
+        const int c = (threadIdx.x + k * blockDim.x) * 4;
+        if (c + 4 <= cols) {
+          mr[k] = ldraw(Mp + c);
+          gr[k] = ldraw_stream(Gp + c);
+          wr[k] = ldraw(Wp + c);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) {
+        float g[4];
+        cvt4(mr[k], v[k]);
+        cvt4(gr[k], g);
+        cvt4(wr[k], w[k]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[k][j] = p.mu * v[k][j] + g[j];
+          ss = fmaf(v[k][j], v[k][j], ss);
+        }
+      }
+    }
+    const float inv = inv_norm_from_sumsq(block_sum(ss, red));
+    if (mt.nz && threadIdx.x == 0 && inv > 0.f) atomicAdd(mt.nz, 1);   // telemetry: nonzero rows
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+      const int c = (threadIdx.x + k * blockDim.x) * 4;
+      if (c + 4 <= cols) {   // cols % 4 == 0 here: a chunk is whole or past the row
+        float o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = w[k][j] - p.eta * (mt.scale * (v[k][j] * inv) + p.lam * w[k][j]);
+        st4(Mp + c, v[k]);
+        st4(Wp + c, o);
+      }
+    }
+  } else {
+    rows_scalar<WT, GT, CPT>(Mp, Gp, Wp, cols, mt.scale, mt.nz, p.mu, p.eta, p.lam, red);
   }
 }
 
@@ -724,6 +831,21 @@ static cudaError_t launch_rows_t(int max_cols, const RowsParams& p, cudaStream_t
   // At most 3-4 four-element chunks per thread keeps registers low and many
   // threads resident; rows up to 16384 columns use at most 1024 threads.
   const int chunks = (max_cols + 3) / 4;
+  // 6145..10240 columns (8192 unless W and G are both bf16: the other five-chunk
+  // kernels spill): rows_wide_kernel, 512 threads
+  if (chunks > 3 * 512 && chunks <= (sizeof(WT) + sizeof(GT) == 4 ? 5 : 4) * 512) {
+    bool vec = true;
+    for (int i = 0; i < p.nmat; ++i) vec = vec && p.mat[i].vec;
+    const dim3 grid(p.total_rows), block(512);
+    if (chunks <= 4 * 512) {
+      if (vec) rows_wide_kernel<WT, GT, 4, true><<<grid, block, 0, s>>>(p);
+      else rows_wide_kernel<WT, GT, 4, false><<<grid, block, 0, s>>>(p);
+    } else {
+      if (vec) rows_wide_kernel<WT, GT, 5, true><<<grid, block, 0, s>>>(p);
+      else rows_wide_kernel<WT, GT, 5, false><<<grid, block, 0, s>>>(p);
+    }
+    return cudaGetLastError();
+  }
   int T = ((chunks + MUON_ROWS_CPT - 1) / MUON_ROWS_CPT + 31) / 32 * 32;
   T = T < 64 ? 64 : (T > 1024 ? 1024 : T);
   const int cpt = (chunks + T - 1) / T;

@@ -12,13 +12,14 @@
 // a separate pass.  In the last iteration the UPDATE epilogue either writes O or
 // applies W <- W - eta*(0.2*sqrt(max(A, B))*O + lambda*W) (Eq. (4)/(7)) directly.
 //
-// Kernel shape: persistent, one CTA per SM, 192 threads.
+// Kernel shape: persistent, one CTA per SM, 320 threads.
 //   warp 0      TMA producer (one lane): 4-stage ring of 128x64 A and 256x64 B
 //               bf16 tiles, 128-byte swizzle;
 //   warp 1      TMEM allocator and MMA issuer (one lane): tcgen05.mma
 //               cta_group::1, M=128, N=256, K=16, two 256-column fp32
 //               accumulators so the epilogue of tile i overlaps the MMAs of i+1;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, fused combine,
+//   warps 2..9  epilogue, two per TMEM lane quarter, each draining 128 of the
+//               256 columns: tcgen05.ld of the accumulator rows, fused combine,
 //               global stores (symmetric outputs are written with their mirror).
 // Tiles of all same-shape matrices (and of several shape groups) form one flat
 // list that CTAs walk with stride gridDim.x.  Every mbarrier wait is bounded in
