@@ -9,7 +9,7 @@
 //    Periodic Row-wise scale).
 //  * rows_kernel: the whole RowNorm step for a wide/square matrix in one pass:
 //    one CTA per row keeps the row in registers (momentum, row norm, apply);
-//    rows_wide_kernel: the same for rows of 6145..10240 columns, shaped for two
+//    rows_wide_kernel: the same for rows of 6145..12288 columns, shaped for two
 //    CTAs per SM.
 //  * apply_kernel: W <- W - eta*(s*U + lambda*W) from a given direction U.
 //  * fro_final_kernel / line_final_kernel: fixed-order reductions of partials.
@@ -367,10 +367,10 @@ rows_kernel(const __grid_constant__ RowsParams p) {
   }
 }
 
-// Rows of 6145..10240 columns: 512 threads with 4-5 four-element chunks each, at
+// Rows of 6145..12288 columns: 512 threads with 4-6 four-element chunks each, at
 // most 64 registers a thread (the 1024-thread bound), so two CTAs per SM and one
 // row's reduction and stores overlap another's loads.  The general kernel above
-// takes up to 864 threads here, one CTA per SM (measured 5.7 against 7.1 TB/s on
+// takes up to 1024 threads here, one CTA per SM (measured 5.7 against 7.1 TB/s on
 // 2560 x 10240 matrices).  The element-load path is a kernel of its own
 // (kVec = false), so that its registers do not count against the vector path.
 //
@@ -831,18 +831,21 @@ static cudaError_t launch_rows_t(int max_cols, const RowsParams& p, cudaStream_t
   // At most 3-4 four-element chunks per thread keeps registers low and many
   // threads resident; rows up to 16384 columns use at most 1024 threads.
   const int chunks = (max_cols + 3) / 4;
-  // 6145..10240 columns (8192 unless W and G are both bf16: the other five-chunk
-  // kernels spill): rows_wide_kernel, 512 threads
-  if (chunks > 3 * 512 && chunks <= (sizeof(WT) + sizeof(GT) == 4 ? 5 : 4) * 512) {
+  // 6145..12288 columns (8192 for fp32 W and G, whose five- and six-chunk kernels
+  // spill): rows_wide_kernel, 512 threads
+  if (chunks > 3 * 512 && chunks <= (sizeof(WT) + sizeof(GT) == 8 ? 4 : 6) * 512) {
     bool vec = true;
     for (int i = 0; i < p.nmat; ++i) vec = vec && p.mat[i].vec;
     const dim3 grid(p.total_rows), block(512);
     if (chunks <= 4 * 512) {
       if (vec) rows_wide_kernel<WT, GT, 4, true><<<grid, block, 0, s>>>(p);
       else rows_wide_kernel<WT, GT, 4, false><<<grid, block, 0, s>>>(p);
-    } else {
+    } else if (chunks <= 5 * 512) {
       if (vec) rows_wide_kernel<WT, GT, 5, true><<<grid, block, 0, s>>>(p);
       else rows_wide_kernel<WT, GT, 5, false><<<grid, block, 0, s>>>(p);
+    } else {
+      if (vec) rows_wide_kernel<WT, GT, 6, true><<<grid, block, 0, s>>>(p);
+      else rows_wide_kernel<WT, GT, 6, false><<<grid, block, 0, s>>>(p);
     }
     return cudaGetLastError();
   }

@@ -139,12 +139,13 @@ def test_rownorm_step_parity(wdt, gdt, path):
     last column block and row block, (40000, 8) has 313 row blocks.  For the cluster
     kernel (40000, 8) takes 16-column strips and (70000, 8) is too tall for its shared
     memory.  (13, 7) and (517, 1) have B % 4 != 0 and take the plain two-pass kernels.
-    Rows of 6145..10240 columns take the 512-thread launch with bf16 W and G: (5, 10240)
-    five whole chunks per thread, (3, 8196) one thread busy in the fifth chunk round,
-    (4, 9999) the element-load kernel; with an fp32 operand these keep the 3-chunk launch."""
+    Rows of 6145..12288 columns take the 512-thread launch unless W and G are both fp32:
+    (5, 10240) five whole chunks per thread, (3, 8196) one thread busy in the fifth chunk
+    round, (2, 12288) six whole chunks, (3, 11000) a part-filled sixth round, (4, 9999) the
+    element-load kernel; with fp32 W and G the widths above 8192 keep the 3-chunk launch."""
     shapes = [(256, 1024), (300, 1000), (1000, 300), (1536, 1536), (7, 13), (13, 7), (1, 517), (517, 1),
               (3, 20000), (129, 129), (4608, 1536), (300, 36), (40000, 8), (70000, 8), (33, 4), (1000, 300),
-              (5, 10240), (3, 8196), (4, 9999)]
+              (5, 10240), (3, 8196), (2, 12288), (3, 11000), (4, 9999)]
     W0, Gs = inputs(shapes, wdt, gdt, 2)
     M0 = rand_M(shapes, seed=8, zero_line=True)
     W = [to_dev(w, wdt) for w in W0]
