@@ -552,7 +552,9 @@ def test_update_norm_refresh_step_parity(dt, mode):
 
 @pytest.mark.parametrize("path", list(TALL_PATHS))
 def test_update_rms_telemetry(path):
-    shapes = [(256, 1024), (1000, 300), (4608, 1536), (1536, 6144), (300, 36), (13, 7), (0, 5), (40000, 8)]
+    # (3, 10240) counts its nonzero rows in the 512-thread wide-row kernel
+    shapes = [(256, 1024), (1000, 300), (4608, 1536), (1536, 6144), (300, 36), (13, 7), (0, 5), (40000, 8),
+              (3, 10240)]
     W0, Gs = inputs(shapes, "bf16", "bf16", 2)
     M0 = rand_M(shapes, seed=21, zero_line=True)
     for i, (a, b) in enumerate(shapes):   # keep the zero line zero through the momentum step
