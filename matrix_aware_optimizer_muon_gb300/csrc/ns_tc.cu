@@ -13,7 +13,8 @@
 // applies W <- W - eta*(0.2*sqrt(max(A, B))*O + lambda*W) (Eq. (4)/(7)) directly.
 //
 // Kernel shape: persistent, one CTA per SM, 320 threads.
-//   warp 0      TMA producer (one lane): 4-stage ring of 128x64 A and 256x64 B
+//   warp 0      TMA producer (one lane): 4-stage ring (3 for POLY and the first
+//               UPDATE) of 128x64 A and 256x64 B
 //               bf16 tiles, 128-byte swizzle;
 //   warp 1      TMEM allocator and MMA issuer (one lane): tcgen05.mma
 //               cta_group::1, M=128, N=256, K=16, two 256-column fp32
@@ -35,7 +36,7 @@ namespace muon {
 namespace tc {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
+constexpr int STAGES = 4;        // mainloop ring depth; 3 for the launches listed at launch_ns_tc
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -43,7 +44,9 @@ constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int EPI_CHUNKS = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per epilogue warp
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+template <int kStages>
+constexpr int smem_bytes() { return kStages * STAGE_BYTES + 1024 + 256; }
+constexpr int SMEM_BYTES = smem_bytes<STAGES>();
 
 struct Tile {
   int g, mat, tm, tn;
@@ -352,14 +355,14 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
 }
 
 // kOsq: the last UPDATE also writes per-warp partial sums of O^2 (only launches
-// that need them pay for them).
-template <bool kOsq>
+// that need them pay for them).  kStages: depth of the TMA/MMA ring.
+template <bool kOsq, int kStages>
 __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_constant__ NsParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * STAGE_BYTES);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* mdone = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
@@ -423,11 +426,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
           }
           pending |= 1u << stage;
           pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
       // drain: every issued copy must land before the CTA may exit
-      for (int s = 0; s < STAGES; ++s)
+      for (int s = 0; s < kStages; ++s)
         if (pending & (1u << s)) wait_bounded(&full[s], (pend_phase >> s) & 1u, abort_flag, p, false);
     }
     __syncwarp();
@@ -465,7 +468,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
             ptx::mma_bf16(d, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           ptx::mma_commit(&empty[stage]);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (stop) break;
         ptx::mma_commit(&tfull[acc]);
@@ -531,15 +534,30 @@ cudaError_t launch_ns_tc(const NsParams& p, cudaStream_t s, int num_sms) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(tc::ns_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    e = cudaFuncSetAttribute(tc::ns_tc_kernel<false, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tc::smem_bytes<4>());
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc::ns_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    e = cudaFuncSetAttribute(tc::ns_tc_kernel<false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tc::smem_bytes<3>());
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(tc::ns_tc_kernel<true, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tc::smem_bytes<4>());
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
-  if (p.osq_part && p.last_iter) tc::ns_tc_kernel<true><<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, s>>>(p);
-  else tc::ns_tc_kernel<false><<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, s>>>(p);
+  // Three stages for POLY and the first UPDATE: the 48 KB of shared memory they free
+  // go to L1, where those launches' epilogue loads gain more than a shallower ring
+  // costs them (per launch on the 1.3B set: POLY 655 -> 584 us, UPDATE 0 4371 -> 4024
+  // us; the long-K Gram product and the later UPDATEs lose 14-15% with three).
+  const bool three = !(p.osq_part && p.last_iter) &&
+                     (p.kind == GEMM_POLY || (p.kind == GEMM_UPDATE && p.first_iter));
+  if (p.osq_part && p.last_iter)
+    tc::ns_tc_kernel<true, 4><<<grid, tc::NUM_THREADS, tc::smem_bytes<4>(), s>>>(p);
+  else if (three)
+    tc::ns_tc_kernel<false, 3><<<grid, tc::NUM_THREADS, tc::smem_bytes<3>(), s>>>(p);
+  else
+    tc::ns_tc_kernel<false, 4><<<grid, tc::NUM_THREADS, tc::smem_bytes<4>(), s>>>(p);
   return cudaGetLastError();
 }
 
