@@ -34,7 +34,7 @@ L2_BYTES = 129e6
 # set (the same shape mix, 1/8 of the matrices) scaled by 8; see
 # profiles/ns_tc_kernel_traffic_mmdit-1.3b.md.  Valid only for the kernel sources
 # it was measured on (hash below); otherwise the roofline reports null.
-NS5_TRAFFIC = {"mmdit-1.3b": {"bytes_per_launch": 4.69e9, "sources": "8bb8d4130fdf103c"}}
+NS5_TRAFFIC = {"mmdit-1.3b": {"bytes_per_launch": 4.73e9, "sources": "bf0c536d7ca75f9d"}}
 NS5_SOURCES = ["ns_tc.cu", "ns_common.cuh", "ptx.cuh", "common.cuh", "internal.h", "api.cu"]
 
 

@@ -142,8 +142,10 @@ bool make_plan(const muon_matrix* mats, int n, int ns5_mode, Plan* P) {
       g.n = mp.n;
       g.m = mp.m;
       g.count = 0;
-      g.ld_n = (int)align_up(mp.n, 8);
-      g.ld_m = (int)align_up(mp.m, 8);
+      // rows padded to 16 elements (32 bytes): the GEMM epilogues move them with
+      // 256-bit accesses
+      g.ld_n = (int)align_up(mp.n, 16);
+      g.ld_m = (int)align_up(mp.m, 16);
       P->groups.push_back(g);
       gi = (int)P->groups.size() - 1;
       open[key].push_back(gi);
@@ -496,7 +498,9 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
             const void* dptr = dst_ptrs ? dst_ptrs[li] : nullptr;
             prm.flags[mbase + q] = (unsigned char)((a.rows > a.cols ? NS_TALL : 0) |
                                                    ((a.cols % 4 == 0 && aligned(a.M, 16)) ? NS_MVEC : 0) |
-                                                   ((a.rows <= a.cols && a.cols % 8 == 0 && aligned(dptr, 16)) ? NS_WVEC : 0));
+                                                   ((a.cols % 8 == 0 && aligned(a.M, 32)) ? NS_MVEC8 : 0) |
+                                                   ((a.rows <= a.cols && a.cols % 8 == 0 && aligned(dptr, 16)) ? NS_WVEC : 0) |
+                                                   ((a.rows <= a.cols && a.cols % 16 == 0 && aligned(dptr, 32)) ? NS_WVEC8 : 0));
           }
           mbase += g.count;
         }

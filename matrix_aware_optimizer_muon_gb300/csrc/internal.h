@@ -230,7 +230,9 @@ struct LineFinalParams {
 // Newton-Schulz GEMMs
 // ---------------------------------------------------------------------------
 enum GemmKind : int { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_UPDATE = 2 };
-enum NsFlags : int { NS_TALL = 1, NS_MVEC = 2, NS_WVEC = 4 };
+// NS_MVEC / NS_WVEC: M rows / the destination's rows take 16-byte vectors; the
+// ...8 forms: 32-byte vectors (256-bit accesses, 32-byte aligned rows).
+enum NsFlags : int { NS_TALL = 1, NS_MVEC = 2, NS_WVEC = 4, NS_MVEC8 = 8, NS_WVEC8 = 16 };
 // Iterations 1..NS_LO_ITERS add a*X_lo, the bf16 residual of X, to (B + aI) X_hi
 // (X carried with ~16 significant bits where the small singular directions are
 // still far below the element magnitudes).
@@ -274,7 +276,7 @@ struct NsParams {
   // last-iteration outputs, per matrix (launch table order)
   void* dst[NS_MAX_MATS];  // W (apply) or O (output)
   const float* msrc[NS_MAX_MATS];  // fp32 momentum, the exact X0 for the first a*X term
-  unsigned char flags[NS_MAX_MATS];  // NS_TALL | NS_MVEC | NS_WVEC
+  unsigned char flags[NS_MAX_MATS];  // NsFlags
   int dst_mode;            // 0: O in dst_dtype; 1: apply to W of dst_dtype;
                            // 2: O to X_out (+ residual) in the workspace
   float* osq_part;         // last UPDATE: partial sums of O^2, [tile][NUM_EPI_WARPS] (or [tile])

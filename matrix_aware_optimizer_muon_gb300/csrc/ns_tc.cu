@@ -109,6 +109,30 @@ __device__ __forceinline__ void store_bf16x32(bf16* dst, const float (&v)[32]) {
     reinterpret_cast<uint4*>(dst)[q] = u;
   }
 }
+
+// 256-bit global accesses (32-byte aligned): a row-per-lane chunk of 64 bytes in two
+// instructions instead of four, so half the L1 requests for the same bytes.
+__device__ __forceinline__ void ld_v8(const void* src, uint32_t* w) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "l"(src));
+}
+__device__ __forceinline__ void st_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+__device__ __forceinline__ void ld_v8x2(const void* src, uint32_t* w) {
+  ld_v8(src, w);
+  ld_v8(reinterpret_cast<const uint8_t*>(src) + 32, w + 8);
+}
+__device__ __forceinline__ void store_bf16x32_v8(bf16* dst, const float (&v)[32]) {
+  uint32_t w[16];
+#pragma unroll
+  for (int h = 0; h < 16; ++h) w[h] = pack_bf16x2(v[2 * h], v[2 * h + 1]);
+  st_v8(dst, w);
+  st_v8(reinterpret_cast<uint8_t*>(dst) + 32, w + 8);
+}
 __device__ __forceinline__ void load_bf16x32(const bf16* src, float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -154,7 +178,7 @@ __device__ __forceinline__ void epi_prefetch(const NsParams& p, const NsGroup& G
   if (p.kind == GEMM_GRAM) return;
   if (p.kind == GEMM_POLY) {
     if (r >= n || c0 + 32 > n || r > c0 + 31) return;
-    ld_u4x4(reinterpret_cast<const bf16*>(G.epi_in) + (size_t)ti.mat * G.stride_nn + (size_t)r * G.ld_n + c0, in.w);
+    ld_v8x2(reinterpret_cast<const bf16*>(G.epi_in) + (size_t)ti.mat * G.stride_nn + (size_t)r * G.ld_n + c0, in.w);
     in.ok = true;
     return;
   }
@@ -164,6 +188,10 @@ __device__ __forceinline__ void epi_prefetch(const NsParams& p, const NsGroup& G
     if (p.flags[gm] & NS_TALL) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) in.w[j] = __float_as_uint(Mp[(size_t)(c0 + j) * n + r]);
+    } else if (p.flags[gm] & NS_MVEC8) {
+      const float* src = Mp + (size_t)r * m + c0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ld_v8(src + 8 * q, in.w + 8 * q);
     } else if (p.flags[gm] & NS_MVEC) {
       const float4* src = reinterpret_cast<const float4*>(Mp + (size_t)r * m + c0);
 #pragma unroll
@@ -179,11 +207,13 @@ __device__ __forceinline__ void epi_prefetch(const NsParams& p, const NsGroup& G
     return;
   }
   const size_t off = (size_t)ti.mat * G.stride_nm + (size_t)r * G.ld_m + c0;
-  if (!p.fold_a) ld_u4x4(reinterpret_cast<const bf16*>(G.epi_in) + off, in.w);
+  if (!p.fold_a) ld_v8x2(reinterpret_cast<const bf16*>(G.epi_in) + off, in.w);
   if (G.lo_in) {
-    ld_u4x4(reinterpret_cast<const bf16*>(G.lo_in) + off, in.w + 16);
+    ld_v8x2(reinterpret_cast<const bf16*>(G.lo_in) + off, in.w + 16);
   } else if (p.last_iter && p.dst_mode == 1 && p.dst_dtype == MUON_DTYPE_BF16) {
-    if (p.flags[gm] & NS_WVEC) {
+    if (p.flags[gm] & NS_WVEC8) {
+      ld_v8x2(reinterpret_cast<const bf16*>(p.dst[gm]) + (size_t)r * m + c0, in.w + 16);
+    } else if (p.flags[gm] & NS_WVEC) {
       ld_u4x4(reinterpret_cast<const bf16*>(p.dst[gm]) + (size_t)r * m + c0, in.w + 16);
     } else if (p.flags[gm] & NS_TALL) {
       // tall W (m x n): W[c][r]; consecutive lanes read consecutive r
@@ -274,8 +304,8 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
 #pragma unroll
       for (int j = 0; j < 32; ++j) lo[j] = v[j] - __bfloat162float(__float2bfloat16_rn(v[j]));
       if (full) {
-        store_bf16x32(Xout, v);
-        if (Lout) store_bf16x32(Lout, lo);
+        store_bf16x32_v8(Xout, v);
+        if (Lout) store_bf16x32_v8(Lout, lo);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -287,15 +317,19 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
     } else {
       const float s_apply = p.rms_match * sqrtf((float)m);
       if (in.ok && p.dst_mode == 1 && p.dst_dtype == MUON_DTYPE_BF16 && (p.flags[gm] & NS_WVEC)) {
-        // wide bf16 W: W[r][c0..c0+31] as four 16-byte vectors
+        // wide bf16 W: W[r][c0..c0+31] as 32- or 16-byte vectors
         float w[32];
         unpack_bf16x32(in.w + 16, w);
 #pragma unroll
         for (int j = 0; j < 32; ++j) w[j] = w[j] - p.eta * (s_apply * v[j] + p.lam * w[j]);
-        store_bf16x32(reinterpret_cast<bf16*>(p.dst[gm]) + (size_t)r * m + c0, w);
+        bf16* Wr = reinterpret_cast<bf16*>(p.dst[gm]) + (size_t)r * m + c0;
+        if (p.flags[gm] & NS_WVEC8) store_bf16x32_v8(Wr, w);
+        else store_bf16x32(Wr, w);
       } else if (p.dst_mode == 0 && p.dst_dtype == MUON_DTYPE_BF16 && full && (p.flags[gm] & NS_WVEC)) {
-        // bf16 O output, wide: row r of O, 32 consecutive columns as 16-byte vectors
-        store_bf16x32(reinterpret_cast<bf16*>(p.dst[gm]) + (size_t)r * m + c0, v);
+        // bf16 O output, wide: row r of O, 32 consecutive columns as 32- or 16-byte vectors
+        bf16* Or = reinterpret_cast<bf16*>(p.dst[gm]) + (size_t)r * m + c0;
+        if (p.flags[gm] & NS_WVEC8) store_bf16x32_v8(Or, v);
+        else store_bf16x32(Or, v);
       } else if (in.ok && p.dst_mode == 1 && p.dst_dtype == MUON_DTYPE_BF16 && (p.flags[gm] & NS_TALL)) {
         // tall bf16 W: element (r, c) of the short-side result is W[c][r]
         float w[32];
@@ -338,7 +372,7 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
   }
   bf16* out = reinterpret_cast<bf16*>(G.out) + (size_t)ti.mat * G.stride_nn;
   if (r <= c0 && c0 + 32 <= n) {
-    store_bf16x32(out + (size_t)r * G.ld_n + c0, v);
+    store_bf16x32_v8(out + (size_t)r * G.ld_n + c0, v);
 #pragma unroll
     for (int j = 0; j < 32; ++j) out[(size_t)(c0 + j) * G.ld_n + r] = __float2bfloat16_rn(v[j]);
   } else {
