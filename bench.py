@@ -1,12 +1,15 @@
 #!/usr/bin/env python
 """Benchmark of the Periodic Row-wise Muon optimizer step on one GB300 (or N replicas).
 
-One bench step = one period of the K = 3 schedule over the whole parameter set:
-an NS5 refresh step followed by two RowNorm steps (every row of the hot path:
-schedule, momentum, Newton-Schulz, RowNorm, scale, apply).  The reported value is
-the mean optimizer-step time (period / 3).  Inputs (W, G, M) are synthetic, on the
-device before the timed region, and larger than L2.  Newton-Schulz GEMM time and
-RowNorm time come from CUDA events that the library records on its stream.
+Default workload: the 15B-class MMDiT parameter set (440 matrices, H = 3072, bf16 W and
+G, fp32 M), the largest set that fits one GPU.  One bench step = one period of the
+K = 3 schedule over the whole set: an NS5 refresh step followed by two RowNorm steps
+(every row of the hot path: schedule, momentum, Newton-Schulz, RowNorm, scale,
+apply).  The reported value is the mean optimizer-step time (period / 3).  Vanilla
+Muon (K = 1, every step a refresh) is timed next, on the same buffers, under the
+`vanilla` key.  Inputs (W, G, M) are synthetic, on the device before the timed region,
+and larger than L2.  Newton-Schulz GEMM time and RowNorm time come from CUDA events
+that the library records on its stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 """
@@ -26,15 +29,16 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Muon optimizer step ms; NS5 TFLOP/s and RowNorm GB/s vs GB300 roofline"
-DEFAULT_WORKLOAD = "mmdit-1.3b"
+# The largest parameter set that fits one GPU (W, G, M and the workspace about 182 GB).
+DEFAULT_WORKLOAD = "mmdit-15b"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129e6
 # DRAM bytes per ns_tc_kernel launch (read + write, averaged over the 15 launches of
-# a refresh), from ncu dram__bytes_{read,write}.sum on the 20-matrix slice of the
-# set (the same shape mix, 1/8 of the matrices) scaled by 8; see
-# profiles/ns_tc_kernel_traffic_mmdit-1.3b.md.  Valid only for the kernel sources
-# it was measured on (hash below); otherwise the roofline reports null.
-NS5_TRAFFIC = {"mmdit-1.3b": {"bytes_per_launch": 4.73e9, "sources": "bf0c536d7ca75f9d"}}
+# a refresh), from ncu dram__bytes_{read,write}.sum on a slice of the set with the
+# same shape mix (whole MMDiT blocks), scaled by the matrix count of the full set.
+# Valid only for the kernel sources it was measured on (hash below); otherwise the
+# roofline reports null.
+NS5_TRAFFIC = {}
 NS5_SOURCES = ["ns_tc.cu", "ns_common.cuh", "ptx.cuh", "common.cuh", "internal.h", "api.cu"]
 
 
@@ -62,6 +66,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--K", type=int, default=0,
                     help="override the schedule period K (1 = vanilla Muon: every step is a refresh)")
+    ap.add_argument("--full-oracle", action="store_true",
+                    help="reference arm: also time the oracle over every matrix of the set for one period")
+    ap.add_argument("--no-vanilla", action="store_true", help="skip the vanilla Muon (K=1) side-by-side timing")
     ap.add_argument("--matrices", type=int, default=0,
                     help="keep only the first N matrices of the set (small cases for profiling)")
     return ap.parse_args()
@@ -81,6 +88,12 @@ def peaks():
 def ns5_flops(shapes):
     """Dense count 5*(4 n^2 m + 2 n^3) per matrix, n = min(A, B), m = max(A, B)."""
     return sum(5 * (4 * min(a, b) ** 2 * max(a, b) + 2 * min(a, b) ** 3) for a, b in shapes)
+
+
+def ns5_flops_symmetric(shapes):
+    """Symmetric-minimum count 5*(3 n^2 m + n^3) per matrix: the two symmetric products
+    (X X^T and S S) counted over one triangle each, the update B X in full."""
+    return sum(5 * (3 * min(a, b) ** 2 * max(a, b) + min(a, b) ** 3) for a, b in shapes)
 
 
 def ns5_flops_executed(shapes):
@@ -192,29 +205,57 @@ def barrier(dist):
 # ---------------------------------------------------------------------------
 # oracle (CPU) timing on a bounded sample
 # ---------------------------------------------------------------------------
-def oracle_sample(wl, seed=0):
-    """One matrix per shape group through one K=3 period with the fp64 oracle.
-    Returns the extrapolated ms per optimizer step for the whole set, and details."""
+def oracle_units(wl):
+    """Units of the oracle sample: one matrix of each shape group on a refresh step and,
+    when K > 1, on a RowNorm step.  Returns (group, rows, cols, count, refresh) tuples."""
+    units = []
+    for gi, ((a, b), cnt) in enumerate(wl.shape_groups()):
+        units.append((gi, a, b, cnt, True))
+        if wl.K > 1:
+            units.append((gi, a, b, cnt, False))
+    return units
+
+
+def time_oracle_unit(wl, unit, seed=0):
+    """Seconds of one fp64 oracle optimizer step on one matrix of the unit's shape (inputs
+    are made before the clock starts)."""
     import numpy as np
     from oracle import muon_ref
     from synth import gradient_np, quantize_np, weight_init_np
-    groups = wl.shape_groups()
+    gi, a, b, _, refresh = unit
+    W = quantize_np(weight_init_np(a, b, seed, gi), wl.w_dtype).astype(np.float64)
+    M = np.zeros((a, b))
+    G = quantize_np(gradient_np(a, b, wl.spike_scales, seed, gi, 0), wl.g_dtype)
+    step = 0 if refresh else 1
+    t0 = time.perf_counter()
+    muon_ref.periodic_step(W, M, G, step, wl.K, wl.gamma, wl.mu, wl.eta, wl.lam, w_dtype=wl.w_dtype)
+    return time.perf_counter() - t0
+
+
+def oracle_extrapolate(wl, times):
+    """ms per optimizer step of the whole set from per-unit seconds ({unit: [s, ...]}):
+    sum over shape groups of count * (refresh + (K - 1) * RowNorm) / K."""
+    per_group = {}
+    for u, ts in times.items():
+        gi, a, b, cnt, refresh = u
+        d = per_group.setdefault(gi, {"shape": [a, b], "count": cnt})
+        d["refresh_s" if refresh else "rownorm_s"] = statistics.mean(ts)
     total = 0.0
     detail = []
-    for gi, ((a, b), cnt) in enumerate(groups):
-        W = quantize_np(weight_init_np(a, b, seed, gi), wl.w_dtype).astype(np.float64)
-        M = np.zeros((a, b))
-        ts = []
-        for step in range(wl.K):
-            G = quantize_np(gradient_np(a, b, wl.spike_scales, seed, gi, step), wl.g_dtype)
-            t0 = time.perf_counter()
-            W, M, _ = muon_ref.periodic_step(W, M, G, step, wl.K, wl.gamma, wl.mu, wl.eta, wl.lam,
-                                             w_dtype=wl.w_dtype)
-            ts.append(time.perf_counter() - t0)
-        total += cnt * sum(ts) / wl.K
-        detail.append({"shape": [a, b], "count": cnt, "refresh_s": round(ts[0], 4),
-                       "rownorm_s": round(sum(ts[1:]) / max(len(ts) - 1, 1), 4)})
+    for gi in sorted(per_group):
+        d = per_group[gi]
+        rn = d.get("rownorm_s", 0.0)
+        total += d["count"] * (d["refresh_s"] + (wl.K - 1) * rn) / wl.K
+        detail.append({"shape": d["shape"], "count": d["count"], "refresh_s": round(d["refresh_s"], 4),
+                       "rownorm_s": round(rn, 4) if wl.K > 1 else None})
     return total * 1e3, detail
+
+
+def oracle_sample_text(wl):
+    return (f"one matrix per shape group ({len(wl.shape_groups())} groups), each timed on one refresh step"
+            + (" and one RowNorm step" if wl.K > 1 else "")
+            + f" of the fp64 oracle; extrapolated by group counts to the {len(wl.matrices)} matrices "
+            f"and the K={wl.K} schedule")
 
 
 def select_workload(args):
@@ -228,31 +269,86 @@ def select_workload(args):
     return wl
 
 
+def config_dict(wl, args, world):
+    """The workload description both arms print (the same keys and values)."""
+    shapes = [(m.rows, m.cols) for m in wl.matrices]
+    wb = 2 if wl.w_dtype == "bf16" else 4
+    gb = 2 if wl.g_dtype == "bf16" else 4
+    in_bytes = sum(-(-(a * b) // 128) * 128 for a, b in shapes) * (wb + gb + 4)
+    flush = in_bytes < 4 * L2_BYTES
+    return {"workload": wl.key, "matrices": len(shapes), "params": wl.n_params,
+            "K": wl.K, "gamma": wl.gamma, "mu": wl.mu, "eta": wl.eta, "lambda": wl.lam,
+            "scale_mode": args.scale_mode,
+            "step": (f"one K={wl.K} period: 1 NS5 refresh + {wl.K - 1} RowNorm optimizer steps; value = period/{wl.K}"
+                     if wl.K > 1 else "vanilla Muon (K=1): every optimizer step is an NS5 refresh"),
+            "l2": (f"inputs larger than L2 (W+G+M {in_bytes / 1e9:.1f} GB vs 129 MB L2), no flush" if not flush
+                   else f"inputs fit in L2 ({in_bytes / 1e6:.1f} MB): L2 flushed (256 MB write) before every "
+                        "timed period; period timed by the library's phase events, excluding the flush"),
+            "parallelism": "replicas" if world > 1 else "single GPU"}, in_bytes, flush
+
+
 def run_reference(args, torch):
+    """The fp64 oracle on the host cores.  One bench step times one unit of the sample
+    (one matrix of one shape group on one branch), in round-robin order over the units;
+    the value extrapolates the per-unit means to the whole set.  Units that --steps does
+    not reach are timed once more after the timed steps, so that every group counts."""
     rank, world, dist = dist_init(torch)
     if rank != 0:
         return
     wl = select_workload(args)
-    for _ in range(min(args.warmup, 1)):   # the oracle needs no more warm-up than one pass
-        oracle_sample(wl)
-    vals = []
-    for _ in range(args.steps):
-        v, detail = oracle_sample(wl)
-        vals.append(v)
-    value = statistics.mean(vals)
-    sample = (f"one matrix per shape group ({len(wl.shape_groups())} groups) through one K={wl.K} period, "
-              f"extrapolated by group counts to {len(wl.matrices)} matrices")
-    cores = os.cpu_count()
+    units = oracle_units(wl)
+    cheapest = min(units, key=lambda u: (u[4], u[1] * u[2]))
+    for _ in range(min(args.warmup, 1)):   # the oracle needs no more warm-up than one import and one call
+        time_oracle_unit(wl, cheapest)
+    times = {u: [] for u in units}
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        u = units[i % len(units)]
+        times[u].append(time_oracle_unit(wl, u))
+    wall = time.perf_counter() - wall0
+    step_s = [t for ts in times.values() for t in ts]
+    extra = [u for u in units if not times[u]]
+    for u in extra:
+        times[u].append(time_oracle_unit(wl, u))
+    value, detail = oracle_extrapolate(wl, times)
+    cfg, _, _ = config_dict(wl, args, 1)
+    sample = oracle_sample_text(wl) + (f"; bench step i times unit i mod {len(units)}"
+                                       + (f"; {len(extra)} units beyond --steps timed once more" if extra else ""))
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "ms", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value * wl.K, 3),
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(statistics.mean(step_s) * 1e3, 3) if step_s else None,
+            "ms_per_step_is": "measured wall time of one bench step (one unit of the sample)",
+            "extrapolated_ms_per_period": round(value * wl.K, 3),
+            "wall_s_timed_steps": round(wall, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": wl.key, "matrices": len(wl.matrices), "params": wl.n_params, "K": wl.K,
-                       "gamma": wl.gamma, "parallelism": "replicas" if args.gpus > 1 else "single process"},
-            "cpu_baseline": {"value": round(value, 3), "unit": "ms", "cores": cores, "kind": "oracle",
+            "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": round(value, 3), "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample, "detail": detail},
             "e2e": {"value": round(value, 3), "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    if args.full_oracle:
+        line["full_oracle"] = full_oracle_period(wl)
     print(json.dumps(line), flush=True)
+
+
+def full_oracle_period(wl, seed=0):
+    """The fp64 oracle over every matrix of the set through one K-step period (no
+    extrapolation): ms per optimizer step."""
+    import numpy as np
+    from oracle import muon_ref
+    from synth import gradient_np, quantize_np, weight_init_np
+    tot = 0.0
+    for i, m in enumerate(wl.matrices):
+        a, b = m.rows, m.cols
+        W = quantize_np(weight_init_np(a, b, seed, i), wl.w_dtype).astype(np.float64)
+        M = np.zeros((a, b))
+        for step in range(wl.K):
+            G = quantize_np(gradient_np(a, b, wl.spike_scales, seed, i, step), wl.g_dtype)
+            t0 = time.perf_counter()
+            W, M, _ = muon_ref.periodic_step(W, M, G, step, wl.K, wl.gamma, wl.mu, wl.eta, wl.lam,
+                                             w_dtype=wl.w_dtype)
+            tot += time.perf_counter() - t0
+    return {"value": round(tot * 1e3 / wl.K, 3), "unit": "ms", "cores": os.cpu_count(),
+            "sample": f"all {len(wl.matrices)} matrices through one K={wl.K} period, timed step by step"}
 
 
 # ---------------------------------------------------------------------------
@@ -324,8 +420,7 @@ def run_ours(args, torch):
     # Sets whose inputs fit in L2 get an L2 flush (a 256 MB write) before every timed
     # period; their period time then comes from the library's own phase events, which
     # exclude the flush.
-    in_bytes = tot * (wb + gb + 4)
-    flush = in_bytes < 4 * L2_BYTES
+    cfg, in_bytes, flush = config_dict(wl, args, world)
     scratch = torch.empty(64 << 20, dtype=torch.float32, device=device) if flush else None
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
@@ -361,10 +456,12 @@ def run_ours(args, torch):
     gpu_launches = launches[0] // args.steps
 
     flops = ns5_flops(shapes)
+    flops_sym = ns5_flops_symmetric(shapes)
     flops_exec = ns5_flops_executed(shapes)
     rn_bytes = rownorm_bytes(shapes, wb, gb)
     pk, pk_src = peaks()
     ns5_tflops = flops / (ns5_ms * 1e-3) / 1e12
+    ns5_sym_tflops = flops_sym / (ns5_ms * 1e-3) / 1e12
     ns5_exec_tflops = flops_exec / (ns5_ms * 1e-3) / 1e12
     rn_gbs = rn_bytes / (rownorm_ms * 1e-3) / 1e9 if has_rn else None
     mom_bytes = momentum_bytes(shapes, gb, 2 if mode == "bf16" else 4)
@@ -382,27 +479,23 @@ def run_ours(args, torch):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(period_ms, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if mode == "bf16" else "f32",
         "data": "synthetic",
-        "config": {"workload": wl.key, "matrices": len(shapes), "params": wl.n_params,
-                   "K": wl.K, "gamma": wl.gamma, "mu": wl.mu, "eta": wl.eta, "lambda": wl.lam,
-                   "scale_mode": args.scale_mode,
-                   "step": (f"one K={wl.K} period: 1 NS5 refresh + {wl.K - 1} RowNorm optimizer steps; value = period/{wl.K}"
-                            if wl.K > 1 else "vanilla Muon (K=1): every optimizer step is an NS5 refresh"),
-                   "l2": (f"inputs larger than L2 (W+G+M {in_bytes / 1e9:.1f} GB vs 129 MB L2), no flush" if not flush
-                          else f"inputs fit in L2 ({in_bytes / 1e6:.1f} MB): L2 flushed (256 MB write) before every "
-                               "timed period; period timed by the library's phase events, excluding the flush"),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": cfg,
         "refresh_ms": round(refresh_ms, 4), "ns5_ms": round(ns5_ms, 4),
         "rownorm_ms": round(rownorm_ms, 4) if has_rn else None,
-        "ns5_tflops": round(ns5_tflops, 1), "ns5_tflops_executed": round(ns5_exec_tflops, 1),
+        "ns5_tflops": round(ns5_sym_tflops, 1), "ns5_tflops_dense": round(ns5_tflops, 1),
+        "ns5_tflops_executed": round(ns5_exec_tflops, 1),
         "rownorm_gbs": round(rn_gbs, 1) if has_rn else None,
         "roofline": ({"kernel": "ns_tc_kernel (Newton-Schulz GEMMs)", "bound": "tensor",
-                      "achieved": round(ns5_tflops, 1), "peak": peak_tc, "unit": "TFLOP/s",
-                      "frac": round(ns5_tflops / peak_tc, 4), "traffic": ns5_traffic,
+                      "achieved": round(ns5_sym_tflops, 1), "peak": peak_tc, "unit": "TFLOP/s",
+                      "frac": round(ns5_sym_tflops / peak_tc, 4), "traffic": ns5_traffic,
+                      "work": "symmetric-minimum count 5*(3 n^2 m + n^3) per matrix (n = min(A,B), m = max(A,B))",
+                      "flops_per_refresh": flops_sym, "launches_per_refresh": n_ns5_launches,
+                      "achieved_dense": round(ns5_tflops, 1), "frac_dense": round(ns5_tflops / peak_tc, 4),
+                      "flops_dense_per_refresh": flops,
                       "achieved_executed": round(ns5_exec_tflops, 1),
                       "frac_executed": round(ns5_exec_tflops / peak_tc, 4),
                       "peak_source": f"{pk_src} bf16_tflops_sustained",
-                      "frac_of_nominal_2250": round(ns5_tflops / 2250.0, 4),
-                      "flops_per_refresh": flops, "launches_per_refresh": n_ns5_launches} if mode == "bf16" else
+                      "frac_of_nominal_2250": round(ns5_sym_tflops / 2250.0, 4)} if mode == "bf16" else
                      {"kernel": "ns_simt_kernel (fp32 Newton-Schulz GEMMs on the CUDA cores)", "bound": "alu",
                       "achieved": round(ns5_tflops, 2), "peak": round(fp32_peak, 1), "unit": "TFLOP/s",
                       "frac": round(ns5_tflops / fp32_peak, 4), "traffic": None,
@@ -421,6 +514,51 @@ def run_ours(args, torch):
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
+
+    # Vanilla Muon (K = 1: every optimizer step an NS5 refresh) on the same buffers,
+    # timed right after the periodic schedule, as the pages compare the two.
+    if wl.K > 1 and not args.no_vanilla:
+        n_v = max(1, args.steps)
+
+        def vstep():
+            mm.muon_periodic_step(W, G, M, step_counter[0], ws, K=1, gamma=wl.gamma, mu=wl.mu, eta=wl.eta,
+                                  lam=wl.lam, ns5_mode=mode, scale_mode=args.scale_mode)
+            step_counter[0] += 1
+
+        for _ in range(max(1, min(args.warmup, 3))):
+            vstep()
+        vevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_v)]
+        for s_ in vevs:
+            for e in s_:
+                e.record()
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        vclocks = ClockSampler(local)
+        vclocks.start()
+        time.sleep(0.3)
+        barrier(dist)
+        torch.cuda.synchronize()
+        v0.record()
+        for i in range(n_v):
+            mm.muon_profile_events(vevs[i])
+            vstep()
+        v1.record()
+        torch.cuda.synchronize()
+        barrier(dist)
+        vclk = vclocks.stop()
+        mm.muon_profile_events([])
+        if mm.muon_check_status(ws) != mm.MUON_OK:
+            raise RuntimeError("device status error in the vanilla Muon steps")
+        v_ms = max_over_ranks(torch, dist, v0.elapsed_time(v1) / n_v, device)
+        v_ns5 = statistics.mean(s_[1].elapsed_time(s_[2]) for s_ in vevs)
+        line["vanilla"] = {
+            "what": "vanilla Muon (K=1, every step an NS5 refresh) on the same buffers, timed after the "
+                    f"K={wl.K} schedule",
+            "ms_per_step": round(v_ms, 4), "steps": n_v, "warmup": max(1, min(args.warmup, 3)),
+            "ns5_ms": round(v_ns5, 4), "ns5_tflops": round(flops_sym / (v_ns5 * 1e-3) / 1e12, 1),
+            "periodic_ms_per_step": line["value"],
+            "optimizer_time_cut": round(1.0 - line["value"] / v_ms, 4),
+            "clocks": vclk}
 
     # End to end through the public API with host buffers (pinned): every optimizer step
     # uploads its gradients and downloads its updated weights inside the timed region.
@@ -477,13 +615,19 @@ def run_ours(args, torch):
 
     e2e_bufs = None
     if not args.no_e2e:
+        torch.cuda.empty_cache()
         free = torch.cuda.mem_get_info(device)[0]
-        for ng, nw in ((3, 2), (2, 1)):   # fewer staging buffers when device memory is short
+        # fewer staging buffers when device memory is short (the 15B set: W, G, M and the
+        # workspace hold about 245 GB); with one G buffer the next upload waits for the
+        # step that reads it, so copies overlap compute less
+        for ng, nw in ((3, 2), (2, 1), (1, 1)):
             if (ng - 1) * tot * gb + nw * tot * wb + (1 << 30) <= free:
                 e2e_bufs = (ng, nw)
                 break
         if e2e_bufs is None:
-            line["e2e"] = {"value": None, "unit": "ms", "skipped": "not enough device memory for the staging buffers"}
+            line["e2e"] = {"value": None, "unit": "ms",
+                           "skipped": f"not enough device memory for the staging buffers ({free / 1e9:.1f} GB free, "
+                                      f"{(tot * wb + (1 << 30)) / 1e9:.1f} GB needed at least)"}
     if e2e_bufs is not None:
         NG, NW = e2e_bufs
         G_host = torch.empty(tot, dtype=gdt, pin_memory=True)
@@ -563,11 +707,11 @@ def run_ours(args, torch):
                                "download); copies_alone_ms: the same copies with no compute"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, detail = oracle_sample(wl)
+        t0c = time.perf_counter()
+        v, detail = oracle_extrapolate(wl, {u: [time_oracle_unit(wl, u)] for u in oracle_units(wl)})
         line["cpu_baseline"] = {"value": round(v, 3), "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": (f"one matrix per shape group ({len(detail)} groups) through one K={wl.K} "
-                                           f"period, extrapolated by group counts to {len(shapes)} matrices"),
-                                "detail": detail}
+                                "sample": oracle_sample_text(wl) + " (each unit timed once)",
+                                "cpu_s": round(time.perf_counter() - t0c, 1), "detail": detail}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
