@@ -29,7 +29,8 @@ Readings where the pages are silent (each also listed in the design doc):
   both branches;
 * refresh iff step % K == 0 with step counted from 0;
 * a zero matrix (for NS5) or a zero line (for RowNorm) gives a zero direction,
-  with no epsilon;
+  with no epsilon; any other norm, NaN or Inf included, divides as written, so
+  non-finite values in M propagate as IEEE arithmetic carries them;
 * the NS5 iteration runs on the short side: a tall matrix is transposed, iterated,
   and transposed back;
 * bf16 storage of W is round-to-nearest-even of the exact fp64 result;
@@ -116,14 +117,18 @@ def rownorm(M: np.ndarray) -> np.ndarray:
     Scaling Muon for Diffusion Transformers, the abstract and the distributed-
     implementation paragraph: each of the min(A, B) lines along the long dimension
     is scaled to unit L2 norm -- the rows of a wide (or square) matrix, the columns
-    of a tall one.  A zero line stays zero.
+    of a tall one.  A zero line stays zero.  Every other line is divided by its norm
+    as written, so a NaN or Inf in a line gives what IEEE division gives (a NaN norm
+    makes the whole line NaN; an Inf norm sends the finite entries to 0).
     """
     M = np.asarray(M, dtype=np.float64)
     A, B = M.shape
     axis = 1 if A <= B else 0          # norm over the long dimension
     norms = np.sqrt(np.sum(M * M, axis=axis, keepdims=True))
-    safe = np.where(norms > 0.0, norms, 1.0)
-    return np.where(norms > 0.0, M / safe, 0.0)
+    zero = norms == 0.0
+    safe = np.where(zero, 1.0, norms)
+    with np.errstate(invalid="ignore"):
+        return np.where(zero, 0.0, M / safe)
 
 
 def update_scale(A: int, B: int, refresh: bool, gamma: float) -> float:

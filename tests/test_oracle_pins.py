@@ -165,6 +165,44 @@ def check_rownorm_bruteforce(o):
         assert np.max(np.abs(R - np.array(want))) < 1e-15
 
 
+def check_nonfinite_propagation(o):
+    """NaN and Inf in the momentum: RowNorm divides every line by its norm as written
+    (brute force with Python floats, whose division is IEEE's: x/inf = 0, inf/inf =
+    nan, x/nan = nan); only an exactly zero line maps to zero.  NS5 of a matrix with
+    one non-finite entry is NaN everywhere: X_0 has a non-finite entry, so X X^T has a
+    non-finite row, and (X X^T)^2 carries it into every entry of B and of B X."""
+    nan, inf = float("nan"), float("inf")
+    for (A, B) in [(3, 6), (6, 3)]:
+        rng = np.random.default_rng(11)
+        M = rng.standard_normal((A, B))
+        if A <= B:
+            M[0, 2] = nan
+            M[1, 4] = inf
+            M[2, :] = 0.0
+        else:
+            M[2, 0] = nan
+            M[4, 1] = -inf
+            M[:, 2] = 0.0
+        R = o.rownorm(M)
+        want = [[0.0] * B for _ in range(A)]
+        lines = range(A) if A <= B else range(B)
+        for l in lines:
+            cells = [(l, j) for j in range(B)] if A <= B else [(i, l) for i in range(A)]
+            nrm = math.sqrt(sum(float(M[i][j]) ** 2 for i, j in cells))
+            for i, j in cells:
+                want[i][j] = float(M[i][j]) / nrm if nrm != 0.0 else 0.0
+        want = np.array(want)
+        assert np.array_equal(np.isnan(R), np.isnan(want))
+        fin = ~np.isnan(want)
+        assert np.max(np.abs(R[fin] - want[fin])) < 1e-15
+        assert np.isnan(R).sum() == (B if A <= B else A) + 1   # the NaN line, and inf/inf
+    for bad in (nan, inf, -inf):
+        M = np.random.default_rng(12).standard_normal((5, 9))
+        M[3, 7] = bad
+        assert np.isnan(o.newton_schulz(M)).all()
+        assert np.isnan(o.newton_schulz(M.T)).all()
+
+
 def check_rownorm_invariants(o):
     rng = np.random.default_rng(7)
     for (A, B) in [(16, 64), (64, 16), (32, 32)]:
@@ -371,7 +409,8 @@ def check_adamw(o):
 
 ALL_CHECKS = [check_constants, check_ns5_closed_form, check_ns5_diagonal, check_ns5_orthogonal_input,
               check_ns5_polar_and_band, check_ns5_short_side, check_ns5_scale_and_zero,
-              check_rownorm_bruteforce, check_rownorm_invariants, check_lemma1, check_momentum,
+              check_rownorm_bruteforce, check_nonfinite_propagation, check_rownorm_invariants, check_lemma1,
+              check_momentum,
               check_apply, check_scale, check_schedule, check_step, check_bf16_rounding, check_update_norm,
               check_update_rms, check_adamw]
 
@@ -407,6 +446,7 @@ MUTATIONS = [
     ("return X.T.copy() if tall else X", "return X"),
     ("NS_B = -4.7750", "NS_B = -4.7705"),
     ("axis = 1 if A <= B else 0", "axis = 1"),
+    ("    zero = norms == 0.0\n", "    zero = ~(norms > 0.0)\n"),
     ("axis = 1 if A <= B else 0", "axis = 1 if A < B else 0"),
     ("return mu * np.asarray(M_prev, dtype=np.float64) + np.asarray(G, dtype=np.float64)",
      "return np.asarray(M_prev, dtype=np.float64) + mu * np.asarray(G, dtype=np.float64)"),
