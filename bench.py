@@ -69,6 +69,8 @@ def parse():
     ap.add_argument("--full-oracle", action="store_true",
                     help="reference arm: also time the oracle over every matrix of the set for one period")
     ap.add_argument("--no-vanilla", action="store_true", help="skip the vanilla Muon (K=1) side-by-side timing")
+    ap.add_argument("--debug-flags", type=int, default=0,
+                    help="library test-hook flags for A/B timing (for example 16: one-CTA Newton-Schulz tiles)")
     ap.add_argument("--matrices", type=int, default=0,
                     help="keep only the first N matrices of the set (small cases for profiling)")
     return ap.parse_args()
@@ -156,7 +158,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, pw = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -167,13 +169,17 @@ class ClockSampler:
                 mx = float(f[2])
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pass
             for nm, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w": statistics.median(pw) if pw else None}
 
 
 # ---------------------------------------------------------------------------
@@ -363,6 +369,8 @@ def run_ours(args, torch):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     mm.load_library()
+    if args.debug_flags:
+        mm.muon_debug_set(args.debug_flags, 0)
     wl = select_workload(args)
     shapes = [(m.rows, m.cols) for m in wl.matrices]
     wdt = torch.bfloat16 if wl.w_dtype == "bf16" else torch.float32
@@ -514,6 +522,8 @@ def run_ours(args, torch):
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
+    if args.debug_flags:
+        line["debug_flags"] = args.debug_flags
 
     # Vanilla Muon (K = 1: every optimizer step an NS5 refresh) on the same buffers,
     # timed right after the periodic schedule, as the pages compare the two.

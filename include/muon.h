@@ -33,11 +33,22 @@
  *    every matrix uses the same (w_dtype, g_dtype) pair.
  *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Every
  *    call only enqueues work on it, never synchronises (except muon_check_status),
- *    and is safe to capture into a CUDA graph.
+ *    and can be captured into a CUDA graph once the one-time set-up has run: the
+ *    first call on a host thread and device creates a second stream and two
+ *    events for that thread, and the first call on a device sets kernel attributes
+ *    and queries occupancy.  Call muon_init() (or make one eager call) on each
+ *    host thread and device before capturing the library's calls.
  *  - Errors: host-side validation happens before any launch; on error nothing is
  *    enqueued and a negative muon_status is returned.  Device-side failures
- *    (bounded waits that expired) are recorded in the workspace's status word and
+ *    (bounded waits that expired; non-finite norms when the finite check of
+ *    muon_periodic_step_ex is on) are recorded in the workspace's status word and
  *    read by muon_check_status().
+ *  - Non-finite values: NaN or Inf in G propagate through the arithmetic as IEEE
+ *    defines it, deterministically.  A NaN or Inf in M makes ||M||_F (a refresh
+ *    step) or that line's norm (a RowNorm step) non-finite; the direction is then
+ *    M divided by that norm, so the whole matrix (refresh) or that line (RowNorm)
+ *    of W becomes NaN, and an Inf norm turns the finite entries' direction into 0.
+ *    Only an exactly zero norm is treated as a zero direction.
  *  - Matrices with A == 0 or B == 0 are accepted and skipped; n == 0 is a no-op.
  *  - Determinism: all reductions use a fixed order, so identical inputs give
  *    bit-identical outputs run to run.
@@ -52,7 +63,7 @@
 extern "C" {
 #endif
 
-#define MUON_ABI_VERSION 1
+#define MUON_ABI_VERSION 2
 
 typedef enum muon_status {
   MUON_OK = 0,
@@ -61,7 +72,9 @@ typedef enum muon_status {
   MUON_ERR_WORKSPACE = -3,   /* workspace null, misaligned or smaller than required */
   MUON_ERR_CUDA = -4,        /* a CUDA runtime or driver call failed */
   MUON_ERR_TIMEOUT = -5,     /* a device-side bounded wait expired (from muon_check_status) */
-  MUON_ERR_NO_DEVICE = -6    /* no usable sm_103 device is current */
+  MUON_ERR_NO_DEVICE = -6,   /* no usable sm_103 device is current */
+  MUON_ERR_NONFINITE = -7    /* a momentum norm was NaN or Inf (from muon_check_status, when the
+                                finite check of muon_periodic_step_ex was on) */
 } muon_status;
 
 enum { MUON_DTYPE_F32 = 0, MUON_DTYPE_BF16 = 1 };
@@ -113,9 +126,12 @@ int muon_fro_norm(const muon_matrix* mats, int n, float* fro_out,
  *    the library, resident on every GPU that loads it until the process exits.
  *  - Limit: at most 2^20 tiles of 64 x 128 elements per call (about 8.6e9
  *    elements of M in total); larger lists return MUON_ERR_UNSUPPORTED.
- *  - The first call on a device looks up the array's device address (once per
- *    device, with that device current); make that first call before any stream
- *    capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress, which allocates nothing); the first call on a device
+ *    may load the library's module there, so make that first call before any
+ *    stream capture.  A device reset is handled: the next call finds the array
+ *    again.
+ *  - Same argument checks and status codes as muon_fro_norm (dtypes included).
  *  - All calls share the array.  Calls that overlap on the GPU (different
  *    streams, or different host threads) race on it; serialise them.
  *  - Allocates nothing, reads M only, writes fro_out[i] = ||M_i||_F.  Does not
@@ -164,6 +180,15 @@ int muon_periodic_step(const muon_matrix* mats, int n, int64_t step, int K, floa
                        float mu, float eta, float lambda, int ns5_mode, void* ws,
                        size_t ws_bytes, muon_stream_t stream, int* branch_out);
 
+/* One-time set-up for the current device and the calling host thread: checks the
+ * device (sm_103), creates the thread's second stream and its fork/join events, sets
+ * the tensor-core kernels' shared-memory attributes and caches occupancy figures.
+ * Every entry point does the same on its first use; calling muon_init first makes
+ * the first step capturable into a CUDA graph.  Allocates no device memory;
+ * repeated calls are cheap no-ops.  Returns MUON_ERR_NO_DEVICE without a usable
+ * device, MUON_ERR_CUDA if a set-up call fails. */
+int muon_init(void);
+
 /* Clears the status header of a fresh workspace (the first 256 bytes) on
  * `stream`.  Call once after allocating a workspace whose contents are not
  * already zero; the rest of the workspace needs no initialisation. */
@@ -182,6 +207,12 @@ typedef struct muon_step_options {
   float* update_rms;   /* optional device array of n floats: RMS of each matrix's direction U
                           (the Newton-Schulz output, or the RowNorm of M) over its A*B elements,
                           as monitored against Lemma 1 ("Muon is Scalable" notes, section 2.2) */
+  int check_finite;    /* nonzero: the kernels that reduce the momentum's norms (||M||_F^2 on a
+                          refresh step, every line's sum of squares on a RowNorm step) set a bit
+                          in the workspace status word when one is NaN or Inf, which
+                          muon_check_status returns as MUON_ERR_NONFINITE.  The check reads
+                          values the step computes anyway: it adds no memory traffic.  The
+                          step's results are the same with the check on or off. */
 } muon_step_options;
 
 /* muon_periodic_step with options (opts == NULL: Eq. (4)/(7) scale, no telemetry).
@@ -218,7 +249,9 @@ int muon_adamw_step(const muon_adamw_param* params, int n, int64_t t, float lr, 
                     double beta2, float eps, float weight_decay, muon_stream_t stream);
 
 /* Synchronises `stream`, reads and clears the device status word in `ws`, and
- * returns MUON_OK or the recorded error (MUON_ERR_TIMEOUT). */
+ * returns MUON_OK or the recorded error: MUON_ERR_TIMEOUT when a bounded wait
+ * expired (it takes precedence), else MUON_ERR_NONFINITE when the finite check saw
+ * a NaN or Inf norm.  The word accumulates over calls until it is read. */
 int muon_check_status(void* ws, size_t ws_bytes, muon_stream_t stream);
 
 /* Profiling hook (process-wide): up to 5 cudaEvent_t handles that
@@ -251,12 +284,15 @@ int muon_abi_version(void);
  * them through the plain two-pass kernels instead, MUON_DEBUG_TALL_CLUSTER
  * through the single-pass thread-block-cluster kernel (to test every path).
  * MUON_DEBUG_NO_OVERLAP runs the wide-row and tall-column kernels of a RowNorm
- * step one after the other on the caller's stream instead of side by side. */
+ * step one after the other on the caller's stream instead of side by side.
+ * MUON_DEBUG_PAIR runs the tensor-core Newton-Schulz GEMMs as 2-CTA clusters
+ * (tcgen05 cta_group::2) on 256 x 256 tiles instead of one CTA per 128 x 256 tile. */
 enum {
   MUON_DEBUG_STALL_PRODUCER = 1,
   MUON_DEBUG_NO_CLUSTER = 2,
   MUON_DEBUG_NO_OVERLAP = 4,
-  MUON_DEBUG_TALL_CLUSTER = 8
+  MUON_DEBUG_TALL_CLUSTER = 8,
+  MUON_DEBUG_PAIR = 16
 };
 int muon_debug_set(int flags, int timeout_ms);
 

@@ -25,6 +25,7 @@ MUON_ERR_WORKSPACE = -3
 MUON_ERR_CUDA = -4
 MUON_ERR_TIMEOUT = -5
 MUON_ERR_NO_DEVICE = -6
+MUON_ERR_NONFINITE = -7
 MUON_DTYPE_F32 = 0
 MUON_DTYPE_BF16 = 1
 MUON_NS5_BF16 = 0
@@ -35,6 +36,7 @@ MUON_DEBUG_STALL_PRODUCER = 1
 MUON_DEBUG_NO_CLUSTER = 2
 MUON_DEBUG_NO_OVERLAP = 4
 MUON_DEBUG_TALL_CLUSTER = 8
+MUON_DEBUG_PAIR = 16
 
 _NS5_MODES = {"bf16": MUON_NS5_BF16, "f32": MUON_NS5_F32}
 
@@ -51,7 +53,7 @@ _SCALE_MODES = {"adjusted_lr": MUON_SCALE_ADJUSTED_LR, "update_norm": MUON_SCALE
 
 
 class MuonStepOptions(ctypes.Structure):
-    _fields_ = [("scale_mode", ctypes.c_int), ("update_rms", ctypes.c_void_p)]
+    _fields_ = [("scale_mode", ctypes.c_int), ("update_rms", ctypes.c_void_p), ("check_finite", ctypes.c_int)]
 
 
 class MuonAdamwParam(ctypes.Structure):
@@ -96,6 +98,7 @@ def load_library(path: Optional[str] = None):
         "muon_check_status": (i32, [vp, sz, vp]),
         "muon_status_str": (ctypes.c_char_p, [i32]),
         "muon_abi_version": (i32, []),
+        "muon_init": (i32, []),
         "muon_debug_set": (i32, [i32, i32]),
         "muon_profile_events": (i32, [ptrs, i32]),
         "muon_adamw_step": (i32, [ctypes.POINTER(MuonAdamwParam), i32, i64, f32, ctypes.c_double, ctypes.c_double,
@@ -261,18 +264,20 @@ def muon_apply(W: Sequence[torch.Tensor], U: Sequence[torch.Tensor], scale_mul: 
 def muon_periodic_step(W: Sequence[torch.Tensor], G: Sequence[torch.Tensor], M: Sequence[torch.Tensor],
                        step: int, ws: torch.Tensor, K: int = 3, gamma: float = 0.15, mu: float = 0.95,
                        eta: float = 0.02, lam: float = 0.01, ns5_mode: str = "bf16", stream=None,
-                       scale_mode: str = "adjusted_lr", update_rms: Optional[torch.Tensor] = None) -> int:
+                       scale_mode: str = "adjusted_lr", update_rms: Optional[torch.Tensor] = None,
+                       check_finite: bool = False) -> int:
     """One Periodic Row-wise Muon step; returns MUON_BRANCH_NS5 or MUON_BRANCH_ROWNORM.
     scale_mode "update_norm" selects Eq. (6); update_rms (n fp32 on the device) receives
-    the RMS of each matrix's direction."""
+    the RMS of each matrix's direction; check_finite makes muon_check_status report
+    MUON_ERR_NONFINITE when a momentum norm of this step was NaN or Inf."""
     arr, n = make_matrices(M, W, G)
     br = ctypes.c_int(-1)
     lib = load_library()
-    if scale_mode == "adjusted_lr" and update_rms is None:
+    if scale_mode == "adjusted_lr" and update_rms is None and not check_finite:
         st = lib.muon_periodic_step(arr, n, int(step), int(K), gamma, mu, eta, lam, _NS5_MODES[ns5_mode],
                                     _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(br))
     else:
-        opts = MuonStepOptions(_SCALE_MODES[scale_mode], _ptr(update_rms))
+        opts = MuonStepOptions(_SCALE_MODES[scale_mode], _ptr(update_rms), 1 if check_finite else 0)
         st = lib.muon_periodic_step_ex(arr, n, int(step), int(K), gamma, mu, eta, lam, _NS5_MODES[ns5_mode],
                                        ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(br))
     _check("muon_periodic_step", st)
@@ -288,6 +293,11 @@ def periodic_step_prepared(arr, n: int, step: int, ws: torch.Tensor, K: int, gam
                                            _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(br))
     _check("muon_periodic_step", st)
     return br.value
+
+
+def muon_init():
+    """One-time set-up of the current device and calling thread (makes the first step capturable)."""
+    _check("muon_init", load_library().muon_init())
 
 
 def muon_debug_set(flags: int = 0, timeout_ms: int = 0):

@@ -129,9 +129,11 @@ bool make_plan(const muon_matrix* mats, int n, int ns5_mode, Plan* P) {
     mp.line_inv = inv_floats;
     inv_floats += mp.lines;
     if (mp.tall) P->tall_chunks += cdiv(mp.B, TALL_CB);
-    // O^2 partials of the last UPDATE: [128x256 tile][8 epilogue warps] or [64x64 tile]
+    // O^2 partials of the last UPDATE: [256x256 pair tile][16 epilogue warps],
+    // [128x256 tile][8 epilogue warps] or [64x64 tile]
     mp.osq = osq_floats;
-    osq_floats += std::max((size_t)cdiv(mp.n, 128) * cdiv(mp.m, 256) * 8, (size_t)cdiv(mp.n, 64) * cdiv(mp.m, 64));
+    osq_floats += std::max({(size_t)cdiv(mp.n, 256) * cdiv(mp.m, 256) * 16, (size_t)cdiv(mp.n, 128) * cdiv(mp.m, 256) * 8,
+                            (size_t)cdiv(mp.n, 64) * cdiv(mp.m, 64)});
     // shape groups of at most NS_MAX_MATS matrices, first-appearance order
     const auto key = std::make_pair(mp.n, mp.m);
     int gi = -1;
@@ -187,9 +189,7 @@ bool make_plan(const muon_matrix* mats, int n, int ns5_mode, Plan* P) {
     g.bm = off;
     off = align_up(off + sb, kAlign);
     const size_t lb = ns5_mode == MUON_NS5_BF16 ? (size_t)g.count * g.n * g.ld_m * 2 : 0;
-    g.lo0 = off;
-    off = align_up(off + lb, kAlign);
-    g.lo1 = off;
+    g.lo = off;
     off = align_up(off + lb, kAlign);
   }
   P->total = off;
@@ -279,7 +279,7 @@ int run_ew(const muon_matrix* mats, const std::vector<int>& idx, int mode, int w
 
 // ||M_i||^2 (and derived values) from the tile partials, fixed order.
 int run_fro_final(const Plan& P, uint8_t* ws, const std::vector<int>& idx, const std::vector<int>& out_idx,
-                  float* fro_sq, float* inv_norm, float* fro, cudaStream_t s) {
+                  float* fro_sq, float* inv_norm, float* fro, cudaStream_t s, unsigned int* status = nullptr) {
   static thread_local FroFinalParams prm;
   size_t k = 0;
   while (k < idx.size()) {
@@ -288,6 +288,7 @@ int run_fro_final(const Plan& P, uint8_t* ws, const std::vector<int>& idx, const
     prm.fro_sq = fro_sq;
     prm.inv_norm = inv_norm;
     prm.fro = fro;
+    prm.status = status;
     int j = 0;
     for (; k < idx.size() && j < FIN_MAX_MATS; ++k, ++j) {
       const MatPlan& mp = P.mats[idx[k]];
@@ -303,11 +304,13 @@ int run_fro_final(const Plan& P, uint8_t* ws, const std::vector<int>& idx, const
   return MUON_OK;
 }
 
-int run_line_final(const Plan& P, uint8_t* ws, const std::vector<int>& idx, cudaStream_t s, int* nz = nullptr) {
+int run_line_final(const Plan& P, uint8_t* ws, const std::vector<int>& idx, cudaStream_t s, int* nz = nullptr,
+                   unsigned int* status = nullptr) {
   static thread_local LineFinalParams prm;
   size_t k = 0;
   while (k < idx.size()) {
     std::memset(&prm, 0, sizeof(prm));
+    prm.status = status;
     int j = 0, lines = 0;
     for (; k < idx.size() && j < LINE_MAX_MATS; ++k) {
       const MatPlan& mp = P.mats[idx[k]];
@@ -396,7 +399,13 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
   std::vector<int> gbase(ng + 1, 0);
   for (int gi = 0; gi < ng; ++gi) gbase[gi + 1] = gbase[gi] + P.groups[gi].count;
   const float* inv_norm_all = reinterpret_cast<const float*>(ws + P.inv_norm);
-  const int slots = tcmode ? 8 : 1;   // O^2 partials per tile: one per epilogue warp, or one per CTA
+  // Tensor-core launches: one CTA per 128 x 256 tile, or 2-CTA clusters on 256 x 256
+  // tiles (MUON_DEBUG_PAIR).  Under the power cap of a long refresh the pair form
+  // draws the clock lower than it gains per clock (15B set: 210.7 -> 233.7 ms per
+  // step at 1680 -> 1367 MHz; 1.3B set: 11.86 -> 11.65 ms).
+  const bool pair = tcmode && (g_debug_flags.load() & MUON_DEBUG_PAIR);
+  // O^2 partials per tile: one per epilogue warp (of both CTAs of a pair), or one per CTA
+  const int slots = tcmode ? (pair ? 16 : 8) : 1;
   long long osq_off = 0;
   if (osq) {
     osq->begin.assign(P.mats.size(), 0);
@@ -427,6 +436,7 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
         prm.status = reinterpret_cast<unsigned int*>(ws + P.status);
         prm.timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;
         prm.debug_flags = g_debug_flags.load();
+        prm.pair = pair ? 1 : 0;
         int tiles = 0, mbase = 0;
         prm.ngroups = ch.second - ch.first;
         for (int gi = ch.first; gi < ch.second; ++gi) {
@@ -450,29 +460,43 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
             G.opB = xin;
             G.epi_in = nullptr;
             G.out = ws + g.s;
-            if (tcmode) { G.mapA = maps[gi].x128[cur]; G.mapB = maps[gi].x256[cur]; }
+            if (tcmode) { G.mapA = maps[gi].x128[cur]; G.mapB = pair ? maps[gi].x128[cur] : maps[gi].x256[cur]; }
           } else if (kind == GEMM_POLY) {
             G.opA = ws + g.s;
             G.opB = ws + g.s;
             G.epi_in = ws + g.s;
             G.out = ws + g.bm;
-            if (tcmode) { G.mapA = maps[gi].s128; G.mapB = maps[gi].s256; }
+            if (tcmode) { G.mapA = maps[gi].s128; G.mapB = pair ? maps[gi].s128 : maps[gi].s256; }
           } else {
             G.opA = ws + g.bm;
             G.opB = xin;
             G.epi_in = xin;
             G.out = xout;
             if (tcmode) {
-              // iteration k writes the residual of X_{k+1} when k < NS_LO_ITERS
-              // and reads the residual of X_k when 1 <= k <= NS_LO_ITERS
-              if (iter < NS_LO_ITERS && iter + 1 < kNsSteps) G.lo_out = ws + ((iter & 1) ? g.lo1 : g.lo0);
-              if (iter >= 1 && iter <= NS_LO_ITERS) G.lo_in = ws + (((iter - 1) & 1) ? g.lo1 : g.lo0);
-              // O kept in the workspace (Eq. (6)): its bf16 residual goes to lo0
-              if (dst_mode == 2 && iter == kNsSteps - 1) G.lo_out = ws + g.lo0;
+              // iteration k writes the residual of X_{k+1} when k < NS_LO_ITERS and reads the
+              // residual of X_k when 1 <= k <= NS_LO_ITERS, both in the one
+              // residual buffer: an epilogue lane reads the element it then overwrites, and
+              // no other tile reads it, so iteration 1 updates the buffer in place
+              if (iter < NS_LO_ITERS && iter + 1 < kNsSteps) G.lo_out = ws + g.lo;
+              if (iter >= 1 && iter <= NS_LO_ITERS) G.lo_in = ws + g.lo;
+              // O kept in the workspace (Eq. (6)): its bf16 residual goes to the same buffer
+              if (dst_mode == 2 && iter == kNsSteps - 1) G.lo_out = ws + g.lo;
             }
             if (tcmode) { G.mapA = maps[gi].b128; G.mapB = maps[gi].x64[cur]; }
           }
-          if (tcmode) {
+          if (tcmode && pair) {
+            // 256 x 256 tiles; the symmetric products take column block tn's row blocks 0..tn
+            G.mtiles = cdiv(g.n, 256);
+            if (kind == GEMM_UPDATE) {
+              G.ntiles = cdiv(g.m, 256);
+              G.tiles_per_mat = G.mtiles * G.ntiles;
+            } else {
+              G.ntiles = cdiv(g.n, 256);
+              int t = 0;
+              for (int tn = 0; tn < G.ntiles; ++tn) t += std::min(tn + 1, G.mtiles);
+              G.tiles_per_mat = t;
+            }
+          } else if (tcmode) {
             G.mtiles = cdiv(g.n, 128);
             if (kind == GEMM_UPDATE) {
               G.ntiles = cdiv(g.m, 256);
@@ -528,7 +552,7 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
 
 // X~ (short-side copy of M) and ||M||^2 partials, then 1/||M|| per matrix.
 int run_ns5_prep(const Plan& P, const muon_matrix* mats, int n, uint8_t* ws, bool momentum, float mu,
-                 int w_dt, int g_dt, cudaStream_t s) {
+                 int w_dt, int g_dt, cudaStream_t s, unsigned int* status = nullptr) {
   std::vector<int> all;
   for (int i = 0; i < n; ++i)
     if (nonempty(mats[i])) all.push_back(i);
@@ -550,7 +574,7 @@ int run_ns5_prep(const Plan& P, const muon_matrix* mats, int n, uint8_t* ws, boo
   std::vector<int> outi(order.size());
   for (size_t k = 0; k < order.size(); ++k) outi[k] = (int)k;
   return run_fro_final(P, ws, order, outi, reinterpret_cast<float*>(ws + P.fro_sq),
-                       reinterpret_cast<float*>(ws + P.inv_norm), nullptr, s);
+                       reinterpret_cast<float*>(ws + P.inv_norm), nullptr, s, status);
 }
 
 int common_checks(int n, DevInfo* di) {
@@ -576,8 +600,18 @@ const char* muon_status_str(int st) {
     case MUON_ERR_CUDA: return "CUDA call failed";
     case MUON_ERR_TIMEOUT: return "device-side wait timed out";
     case MUON_ERR_NO_DEVICE: return "no sm_103 device is current";
+    case MUON_ERR_NONFINITE: return "a momentum norm was NaN or Inf";
     default: return "unknown status";
   }
+}
+
+int muon_init(void) {
+  DevInfo di;
+  int rc = device_info(&di);
+  if (rc != MUON_OK) return rc;
+  if (!aux_stream()) return MUON_ERR_CUDA;
+  if (prepare_ns_tc() != cudaSuccess || prepare_tall() != cudaSuccess) return MUON_ERR_CUDA;
+  return MUON_OK;
 }
 
 int muon_debug_set(int flags, int timeout_ms) {
@@ -610,7 +644,7 @@ int muon_check_status(void* ws, size_t ws_bytes, muon_stream_t stream) {
   if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MUON_ERR_CUDA;
   if (word != 0) {
     if (cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return MUON_ERR_CUDA;
-    return MUON_ERR_TIMEOUT;
+    return (word & DEV_TIMEOUT) ? MUON_ERR_TIMEOUT : MUON_ERR_NONFINITE;
   }
   return MUON_OK;
 }
@@ -772,6 +806,7 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
   if (ns5_mode != MUON_NS5_BF16 && ns5_mode != MUON_NS5_F32) return MUON_ERR_UNSUPPORTED;
   const int scale_mode = opts ? opts->scale_mode : MUON_SCALE_ADJUSTED_LR;
   float* update_rms = opts ? opts->update_rms : nullptr;
+  const bool check_finite = opts && opts->check_finite;
   if (scale_mode != MUON_SCALE_ADJUSTED_LR && scale_mode != MUON_SCALE_UPDATE_NORM) return MUON_ERR_UNSUPPORTED;
   if (update_rms && !aligned(update_rms, 4)) return MUON_ERR_INVALID;
   Check ck;
@@ -789,10 +824,12 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
   if ((rc = check_ws(P, ws, ws_bytes)) != MUON_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
+  // finite check: the kernels that reduce the momentum's norms report NaN or Inf here
+  unsigned int* fin_status = check_finite ? reinterpret_cast<unsigned int*>(w + P.status) : nullptr;
 
   if (refresh) {
     prof_record(0, s);
-    rc = run_ns5_prep(P, mats, n, w, true, mu, ck.w_dt, ck.g_dt, s);
+    rc = run_ns5_prep(P, mats, n, w, true, mu, ck.w_dt, ck.g_dt, s, fin_status);
     if (rc != MUON_OK) return rc;
     std::vector<void*> dst(n);
     for (int i = 0; i < n; ++i) dst[i] = mats[i].W;
@@ -843,7 +880,7 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
             const size_t moff = (size_t)mp.idx_in_group * g.n * g.ld_m;
             e.W = mats[k].W;
             e.O = w + g.x1 + moff * esize;                       // output of the last UPDATE
-            e.O_lo = tc ? (const void*)(w + g.lo0 + moff * 2) : nullptr;
+            e.O_lo = tc ? (const void*)(w + g.lo + moff * 2) : nullptr;
             if (tc && mp.tall) {
               // the tensor-core path wrote a tall matrix's O in W's orientation
               // (m x n, leading dimension n): an elementwise pass over W
@@ -910,6 +947,7 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
       rp.mu = mu;
       rp.eta = eta;
       rp.lam = lambda;
+      rp.status = fin_status;
       int j = 0, rows = 0;
       for (; k < v.size() && j < ROWS_MAX_MATS; ++k) {
         const muon_matrix& a = mats[v[k]];
@@ -982,6 +1020,7 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
         tp.status = reinterpret_cast<unsigned int*>(w + P.status);
         tp.timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;
         tp.stall = (dbg & MUON_DEBUG_STALL_PRODUCER) ? 1 : 0;
+        tp.check_finite = check_finite ? 1 : 0;
         if (cudaMemsetAsync(ctrl, 0, sizeof(unsigned) * (size_t)tall_ctrl_words(tp.nchunks), s) != cudaSuccess)
           return MUON_ERR_CUDA;
         if ((rc = cuda_status(launch_tall(ck.w_dt, ck.g_dt, tp, di.sms, s))) != MUON_OK) return rc;
@@ -1012,6 +1051,7 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
         cp.eta = eta;
         cp.lam = lambda;
         cp.slab_max = (kv.first + cols_cluster_size() - 1) / cols_cluster_size();
+        cp.status = fin_status;
         int j = 0, units = 0;
         for (; k < v.size() && j < COLS_MAX_MATS; ++k) {
           const muon_matrix& a = mats[v[k]];
@@ -1050,7 +1090,7 @@ int muon_periodic_step_ex(const muon_matrix* mats, int n, int64_t step, int K, f
     rc = run_ew(mats, two_pass, EW_MOMENTUM | EW_LINEPART, ck.w_dt, ck.g_dt, MUON_DTYPE_F32, mu, eta, lambda,
                 fill, s);
     if (rc != MUON_OK) return rc;
-    rc = run_line_final(P, w, two_pass, s, nz);
+    rc = run_line_final(P, w, two_pass, s, nz, fin_status);
     if (rc != MUON_OK) return rc;
     rc = run_ew(mats, two_pass, EW_APPLY_LINE, ck.w_dt, ck.g_dt, MUON_DTYPE_F32, mu, eta, lambda, fill, s);
     if (rc != MUON_OK) return rc;

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(NT, 2) cols_cluster_kernel(const __grid_consta
     float t = 0.f;
 #pragma unroll
     for (int q = 0; q < CL; ++q) t += dsmem_ld(&colpart[threadIdx.x], (uint32_t)q);
+    if (rank == 0 && c0 + (int)threadIdx.x < B) note_nonfinite(p.status, t);
     inv[threadIdx.x] = inv_norm_from_sumsq(t);
   }
   __syncthreads();

@@ -105,8 +105,10 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 __device__ __forceinline__ float inv_norm_from_sumsq(float ss) {
-  // zero line or zero matrix -> zero direction (no epsilon)
-  return ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+  // An exactly zero line or matrix gives a zero direction (no epsilon).  Any other
+  // sum is divided through as it is: NaN stays NaN and Inf gives 0, so a non-finite
+  // momentum propagates into the direction as the division M/||M|| defines it.
+  return ss == 0.f ? 0.f : 1.0f / sqrtf(ss);
 }
 
 }  // namespace muon

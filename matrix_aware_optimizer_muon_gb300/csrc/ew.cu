@@ -348,7 +348,9 @@ rows_kernel(const __grid_constant__ RowsParams p) {
       for (int j = 0; j < 4; ++j) ss = fmaf(v[k][j], v[k][j], ss);
     }
   }
-  const float inv = inv_norm_from_sumsq(block_sum(ss, red));
+  const float sst = block_sum(ss, red);
+  if (threadIdx.x == 0) note_nonfinite(p.status, sst);
+  const float inv = inv_norm_from_sumsq(sst);
   if (mt.nz && threadIdx.x == 0 && inv > 0.f) atomicAdd(mt.nz, 1);   // telemetry: nonzero rows
 #pragma unroll
   for (int k = 0; k < CPT; ++k) {
@@ -378,7 +380,7 @@ rows_kernel(const __grid_constant__ RowsParams p) {
 template <typename WT, typename GT, int CPT>
 __device__ __forceinline__ void rows_scalar(float* __restrict__ Mp, const GT* __restrict__ Gp, WT* __restrict__ Wp,
                                          int cols, float scale, int* nz, float mu, float eta, float lam,
-                                         float* red) {
+                                         float* red, unsigned int* status) {
   float v[CPT][4], w[CPT][4];
   float ss = 0.f;
 #pragma unroll
@@ -393,7 +395,9 @@ __device__ __forceinline__ void rows_scalar(float* __restrict__ Mp, const GT* __
 #pragma unroll
     for (int j = 0; j < 4; ++j) ss = fmaf(v[k][j], v[k][j], ss);
   }
-  const float inv = inv_norm_from_sumsq(block_sum(ss, red));
+  const float sst = block_sum(ss, red);
+  if (threadIdx.x == 0) note_nonfinite(status, sst);
+  const float inv = inv_norm_from_sumsq(sst);
   if (nz && threadIdx.x == 0 && inv > 0.f) atomicAdd(nz, 1);   // telemetry: nonzero rows
 #pragma unroll
   for (int k = 0; k < CPT; ++k) {
@@ -454,7 +458,9 @@ rows_wide_kernel(const __grid_constant__ RowsParams p) {
         }
       }
     }
-    const float inv = inv_norm_from_sumsq(block_sum(ss, red));
+    const float sst = block_sum(ss, red);
+    if (threadIdx.x == 0) note_nonfinite(p.status, sst);
+    const float inv = inv_norm_from_sumsq(sst);
     if (mt.nz && threadIdx.x == 0 && inv > 0.f) atomicAdd(mt.nz, 1);   // telemetry: nonzero rows
 #pragma unroll
     for (int k = 0; k < CPT; ++k) {
@@ -468,7 +474,7 @@ rows_wide_kernel(const __grid_constant__ RowsParams p) {
       }
     }
   } else {
-    rows_scalar<WT, GT, CPT>(Mp, Gp, Wp, cols, mt.scale, mt.nz, p.mu, p.eta, p.lam, red);
+    rows_scalar<WT, GT, CPT>(Mp, Gp, Wp, cols, mt.scale, mt.nz, p.mu, p.eta, p.lam, red, p.status);
   }
 }
 
@@ -566,6 +572,7 @@ fro_final_kernel(const __grid_constant__ FroFinalParams p) {
   if (threadIdx.x == 0) {
     const int o = p.out_index[i];
     const float ss = (float)s;
+    note_nonfinite(p.status, ss);
     if (p.fro_sq) p.fro_sq[o] = ss;
     if (p.inv_norm) p.inv_norm[o] = inv_norm_from_sumsq(ss);
     if (p.fro) p.fro[o] = sqrtf(ss);
@@ -586,6 +593,7 @@ line_final_kernel(const __grid_constant__ LineFinalParams p) {
   const int l = g - mt.line_begin;
   double s = 0.0;
   for (int q = 0; q < mt.parts; ++q) s += (double)mt.part[(size_t)q * mt.lines + l];
+  note_nonfinite(p.status, (float)s);
   const float inv = inv_norm_from_sumsq((float)s);
   mt.inv[l] = inv;
   if (mt.nz && inv > 0.f) atomicAdd(mt.nz, 1);   // telemetry: nonzero lines

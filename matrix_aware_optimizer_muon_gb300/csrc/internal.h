@@ -73,6 +73,7 @@ struct RowsParams {
   int nmat;
   int total_rows;
   float mu, eta, lam;
+  unsigned int* status;    // finite check: DEV_NONFINITE when a row norm is NaN or Inf (null: off)
 };
 
 // single-pass RowNorm step for tall matrices: one thread-block cluster per
@@ -95,6 +96,7 @@ struct ColsParams {
   int total_units;
   int slab_max;            // rows per CTA slab (ceil(max rows / cluster size))
   float mu, eta, lam;
+  unsigned int* status;    // finite check: DEV_NONFINITE when a column norm is NaN or Inf (null: off)
 };
 
 // RowNorm step for tall matrices as two row-contiguous passes (tall.cu): chunks
@@ -133,10 +135,20 @@ struct TallParams {
   unsigned int* status;    // workspace status word
   unsigned long long timeout_ns;
   int stall;               // test hook: publish no column norms, so that pass 2 times out
+  int check_finite;        // finite check: DEV_NONFINITE in *status when a column norm is NaN or Inf
 };
 
-// Status-word bit set by a kernel whose bounded wait expired.
+// Status-word bits: a kernel's bounded wait expired; a momentum norm was NaN or Inf
+// (recorded only when the caller asked for the finite check).
 constexpr uint32_t DEV_TIMEOUT = 1u;
+constexpr uint32_t DEV_NONFINITE = 2u;
+
+#ifdef __CUDACC__
+// Finite check of a sum of squares of the momentum (status null: check off).
+__device__ __forceinline__ void note_nonfinite(unsigned int* status, float ss) {
+  if (status && !isfinite(ss)) atomicOr(status, DEV_NONFINITE);
+}
+#endif
 
 // apply from a given direction U
 constexpr int APPLY_MAX_MATS = 128;
@@ -167,6 +179,7 @@ struct FroFinalParams {
   float* fro_sq;              // optional outputs, indexed by out_index
   float* inv_norm;
   float* fro;
+  unsigned int* status;       // finite check: DEV_NONFINITE when a ||M||^2 is NaN or Inf (null: off)
 };
 constexpr int LINE_MAX_MATS = 256;
 struct LineFinalMat {
@@ -224,6 +237,7 @@ struct LineFinalParams {
   LineFinalMat mat[LINE_MAX_MATS];
   int nmat;
   int total_lines;
+  unsigned int* status;       // finite check: DEV_NONFINITE when a line norm is NaN or Inf (null: off)
 };
 
 // ---------------------------------------------------------------------------
@@ -285,6 +299,8 @@ struct NsParams {
   unsigned int* status;    // device status word
   unsigned long long timeout_ns;
   int debug_flags;
+  int pair;                // tensor-core path: 2-CTA clusters on 256 x 256 tiles (mtiles counts
+                           // 256-row blocks), else one CTA per 128 x 256 tile
 };
 
 // ---------------------------------------------------------------------------
@@ -311,7 +327,7 @@ struct GroupPlan {
   std::vector<int> mats;   // indices into the matrix list
   int ld_n, ld_m;
   size_t x0, x1, s, bm;    // byte offsets in the workspace
-  size_t lo0, lo1;         // bf16 residual ping-pong (tensor-core mode only)
+  size_t lo;               // bf16 residual of X (tensor-core mode only), updated in place
 };
 
 struct Plan {
@@ -339,6 +355,10 @@ cudaError_t launch_apply(int w_dt, int u_dt, const ApplyParams& p, cudaStream_t 
 cudaError_t launch_cols(int w_dt, int g_dt, int cw, const ColsParams& p, cudaStream_t s);
 cudaError_t launch_tall(int w_dt, int g_dt, const TallParams& p, int num_sms, cudaStream_t s);
 int tall_ctrl_words(int nchunks);
+// one-time set-up of the current device (kernel attributes, occupancy), process-wide
+cudaError_t prepare_ns_tc();
+int ns_tc_pairs();          // co-resident 2-CTA clusters of the pair kernel on the current device
+cudaError_t prepare_tall();
 int cols_cluster_size();
 int cols_strip_width(int max_rows, int stage_elem_bytes);
 cudaError_t launch_fro_final(const FroFinalParams& p, cudaStream_t s);

@@ -11,7 +11,6 @@
 // The kernels are the same ones muon_fro_norm launches; only the scratch address
 // differs.
 #include <cstring>
-#include <mutex>
 #include <vector>
 
 #include "common.cuh"
@@ -26,27 +25,22 @@ constexpr int kNoallocMaxPartials = 1 << 20;  // 64 x 128 tiles, i.e. up to ~8.6
 // written earlier in the same call, so nothing needs clearing between calls.
 static __device__ __align__(256) float g_noalloc_partials[kNoallocMaxPartials];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-float* g_scratch[kMaxDevices] = {};
-
-// Device address of the scratch array for the current device (looked up once per
-// device; the host-side symbol itself is not a device address).
+// Device address of the scratch array on the current device.  The host-side symbol
+// itself is not a device address.  The address is looked up on every call rather
+// than cached: a device reset or a new primary context reloads the module, and the
+// array may then sit elsewhere.  The lookup does not allocate; on the first call on a
+// device it may load the library's module there.
 int scratch_for_current_device(float** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MUON_ERR_NO_DEVICE;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return MUON_ERR_NO_DEVICE;
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return MUON_ERR_NO_DEVICE;
   if (major != 10 || minor != 3) return MUON_ERR_NO_DEVICE;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return MUON_ERR_CUDA;
-    g_scratch[dev] = static_cast<float*>(p);
-  }
-  *out = g_scratch[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return MUON_ERR_CUDA;
+  *out = static_cast<float*>(p);
   return MUON_OK;
 }
 
@@ -65,6 +59,10 @@ extern "C" int muon_fro_norm_noalloc(const muon_matrix* mats, int n, float* fro_
   for (int i = 0; i < n; ++i) {
     const muon_matrix& a = mats[i];
     if (a.rows < 0 || a.cols < 0 || a.rows >= (1LL << 31) || a.cols >= (1LL << 31)) return MUON_ERR_INVALID;
+    // the same dtype rules as every other entry point (muon_fro_norm returns the same status)
+    if (a.w_dtype != MUON_DTYPE_F32 && a.w_dtype != MUON_DTYPE_BF16) return MUON_ERR_UNSUPPORTED;
+    if (a.g_dtype != MUON_DTYPE_F32 && a.g_dtype != MUON_DTYPE_BF16) return MUON_ERR_UNSUPPORTED;
+    if (a.w_dtype != mats[0].w_dtype || a.g_dtype != mats[0].g_dtype) return MUON_ERR_UNSUPPORTED;
     if (a.rows == 0 || a.cols == 0) continue;
     if (!a.M || reinterpret_cast<uintptr_t>(a.M) % 4 != 0) return MUON_ERR_INVALID;
     total_tiles += (long long)cdiv_i(a.rows, TILE_R) * cdiv_i(a.cols, TILE_C);

@@ -27,6 +27,9 @@
 // time; on expiry the kernel records MUON_DEV_TIMEOUT in the status word, all
 // roles stop, in-flight copies and MMAs are drained (again bounded) and TMEM is
 // freed before exit.
+#include <map>
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -557,27 +560,300 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
   if (warp == 1) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair form (tcgen05 cta_group::2): a 2-CTA cluster computes a 256 x 256 output
+// tile.  The even CTA issues every MMA (M = 256, N = 256, K = 16); each CTA stages
+// its own 128 rows of A and 128 columns (N) of B per K step, 32 KB a stage instead
+// of 48, so the same shared memory holds half again as many K steps in flight, and
+// each CTA's tensor memory receives its 128 rows of the tile, drained by its own
+// epilogue warps exactly as in the one-CTA form.
+//   full[s]   (even CTA): the producers of both CTAs land their halves on it; the
+//             even producer posts the expected bytes of both;
+//   empty[s]  (both CTAs): the MMA commit arrives on both, multicast;
+//   tfull[a]  (both CTAs): the tile's last commit, multicast;
+//   tempty[a] (even CTA): the 16 epilogue warps of both CTAs arrive on it.
+// ---------------------------------------------------------------------------
+constexpr int P_A_BYTES = BM * BK * 2;            // this CTA's 128 rows of A
+constexpr int P_B_BYTES = (BN / 2) * BK * 2;      // this CTA's 128 columns of B
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+template <int kStages>
+constexpr int smem_bytes_pair() { return kStages * P_STAGE_BYTES + 1024 + 256; }
+
+// Pair tiles: G.mtiles counts 256-row blocks.  ti.tm is this CTA's 128-row block.
+__device__ __forceinline__ Tile decode_pair(const NsParams& p, int t, int rank) {
+  Tile ti;
+  int g = 0;
+  while (g + 1 < p.ngroups && p.g[g + 1].tile_begin <= t) ++g;
+  const NsGroup& G = p.g[g];
+  const int lt = t - G.tile_begin;
+  ti.g = g;
+  ti.mat = lt / G.tiles_per_mat;
+  int r = lt - ti.mat * G.tiles_per_mat;
+  int tp;
+  if (p.kind == GEMM_UPDATE) {
+    ti.tn = r / G.mtiles;
+    tp = r - ti.tn * G.mtiles;
+  } else {
+    // upper-triangle 256 x 256 tiles: column block tn holds row blocks 0 .. tn
+    int tn = 0;
+    while (true) {
+      const int cnt = min(tn + 1, G.mtiles);
+      if (r < cnt) break;
+      r -= cnt;
+      ++tn;
+    }
+    ti.tn = tn;
+    tp = r;
+  }
+  ti.tm = 2 * tp + rank;
+  return ti;
+}
+
+template <bool kOsq, int kStages>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    ns_tc_pair_kernel(const __grid_constant__ NsParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * P_STAGE_BYTES);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mdone = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)ptx::cluster_ctarank();
+  const bool even = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 2 * NUM_EPI_WARPS);
+    }
+    ptx::mbar_init(mdone, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();   // both CTAs' barriers initialised and tensor memory allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  const int kind = p.kind;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0 && !(p.debug_flags & MUON_DEBUG_STALL_PRODUCER)) {
+      for (int g = 0; g < p.ngroups; ++g) {
+        ptx::prefetch_tmap(&p.g[g].mapA);
+        ptx::prefetch_tmap(&p.g[g].mapB);
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t pending = 0, pend_phase = 0;
+      bool stop = false;
+      for (int t = pair; t < p.total_tiles && !stop; t += npairs) {
+        const Tile ti = decode_pair(p, t, rank);
+        const NsGroup& G = p.g[ti.g];
+        const int K = (kind == GEMM_GRAM) ? G.m : G.n;
+        const int nkb = (K + BK - 1) / BK;
+        const int n0 = ti.tn * BN + rank * (BN / 2);   // this CTA's half of the N columns
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p, true)) { stop = true; break; }
+          const uint32_t fb = ptx::mapa_shared(ptx::smem_addr(&full[stage]), 0);
+          if (even) ptx::mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+          const uint32_t sa = ptx::smem_addr(smem + stage * P_STAGE_BYTES);
+          const uint32_t sb = sa + P_A_BYTES;
+          const int k0 = kb * BK;
+          ptx::tma_load_3d_pair(sa, &G.mapA, fb, k0, ti.tm * BM, ti.mat);
+          if (kind == GEMM_UPDATE) {
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              ptx::tma_load_3d_pair(sb + j * (64 * BK * 2), &G.mapB, fb, n0 + 64 * j, k0, ti.mat);
+          } else {
+            ptx::tma_load_3d_pair(sb, &G.mapB, fb, k0, n0, ti.mat);
+          }
+          pending |= 1u << stage;
+          pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // drain: the even CTA's full barriers count both CTAs' copies; the odd CTA's
+      // copies have landed once the even CTA has seen them (it waits at the final
+      // cluster barrier for that)
+      if (even)
+        for (int s = 0; s < kStages; ++s)
+          if (pending & (1u << s)) wait_bounded(&full[s], (pend_phase >> s) & 1u, abort_flag, p, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (even && lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, BN, false, kind == GEMM_UPDATE);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool stop = false;
+      for (int t = pair; t < p.total_tiles && !stop; t += npairs, ++it) {
+        const Tile ti = decode_pair(p, t, 0);
+        const NsGroup& G = p.g[ti.g];
+        const int K = (kind == GEMM_GRAM) ? G.m : G.n;
+        const int nkb = (K + BK - 1) / BK;
+        const int acc = it & 1;
+        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, p, true)) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&full[stage], phase, abort_flag, p, true)) { stop = true; break; }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_addr(smem + stage * P_STAGE_BYTES);
+          const uint32_t sb = sa + P_A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t adesc = ptx::smem_desc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bdesc = (kind == GEMM_UPDATE) ? ptx::smem_desc_sw128(sb + k * 2048, 64 * BK * 2, 1024)
+                                                         : ptx::smem_desc_sw128(sb + k * 32, 16, 1024);
+            ptx::mma_bf16_pair(d, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit_pair_mc(&empty[stage], 3);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (stop) break;
+        ptx::mma_commit_pair_mc(&tfull[acc], 3);
+      }
+      // drain: all issued MMAs complete before either CTA releases its tensor memory
+      ptx::mma_commit_pair_mc(mdone, 1);
+      wait_bounded(mdone, 0, abort_flag, p, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row_in_tile = quarter * 32 + lane;
+    int it = 0;
+    for (int t = pair; t < p.total_tiles; t += npairs, ++it) {
+      const Tile ti = decode_pair(p, t, rank);
+      const NsGroup& G = p.g[ti.g];
+      const int acc = it & 1;
+      const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      const int r = ti.tm * BM + row_in_tile;
+      const int cbase = ti.tn * BN + half * (EPI_CHUNKS * 32);
+      ChunkIn in[2];
+      float osq = 0.f;
+      epi_prefetch(p, G, ti, r, cbase, in[0]);
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, p, true) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * EPI_CHUNKS * 32);
+#pragma unroll
+      for (int k = 0; k < EPI_CHUNKS; ++k) {
+        float v[32];
+        ptx::tmem_ld_32x32b_x32(tbase + k * 32, v);
+        if (k + 1 < EPI_CHUNKS) epi_prefetch(p, G, ti, r, cbase + (k + 1) * 32, in[(k + 1) & 1]);
+        epi_finish<kOsq>(p, G, ti, r, cbase + k * 32, v, in[k & 1], osq);
+      }
+      if (kOsq && p.last_iter) {   // one fixed slot per (pair tile, CTA, epilogue warp)
+        osq = warp_sum(osq);
+        if (lane == 0) p.osq_part[((size_t)t * 2 + rank) * NUM_EPI_WARPS + (warp - 2)] = osq;
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (even) ptx::mbar_arrive(&tempty[acc]);
+        else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_addr(&tempty[acc]), 0));
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  ptx::cluster_sync();   // no CTA leaves while its pair may still read its shared memory
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
 }  // namespace tc
 
 int ns_tc_smem_bytes() { return tc::SMEM_BYTES; }
 
-cudaError_t launch_ns_tc(const NsParams& p, cudaStream_t s, int num_sms) {
-  if (p.total_tiles <= 0) return cudaSuccess;
-  static thread_local int configured_device = -1;
+// Kernel attributes (dynamic shared memory beyond 48 KB) apply per device for the
+// whole process: set once per device, under a lock, with the number of CTA pairs
+// that fit on the device at once.
+namespace {
+std::mutex g_tc_mu;
+std::map<int, int> g_tc_pairs;   // device -> co-resident 2-CTA clusters
+#ifndef MUON_PAIR_STAGES
+#define MUON_PAIR_STAGES 6
+#endif
+constexpr int kPairStages = MUON_PAIR_STAGES;
+}  // namespace
+
+cudaError_t prepare_ns_tc() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(tc::ns_tc_kernel<false, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tc::smem_bytes<4>());
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc::ns_tc_kernel<false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tc::smem_bytes<3>());
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc::ns_tc_kernel<true, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tc::smem_bytes<4>());
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
+  std::lock_guard<std::mutex> lk(g_tc_mu);
+  if (g_tc_pairs.count(dev)) return cudaSuccess;
+  e = cudaFuncSetAttribute(tc::ns_tc_kernel<false, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::smem_bytes<4>());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::ns_tc_kernel<false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::smem_bytes<3>());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::ns_tc_kernel<true, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::smem_bytes<4>());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::ns_tc_pair_kernel<false, kPairStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::smem_bytes_pair<kPairStages>());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::ns_tc_pair_kernel<true, kPairStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::smem_bytes_pair<kPairStages>());
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(tc::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = tc::smem_bytes_pair<kPairStages>();
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, tc::ns_tc_pair_kernel<false, kPairStages>, &cfg);
+  if (e != cudaSuccess) return e;
+  g_tc_pairs[dev] = clusters;
+  return cudaSuccess;
+}
+
+int ns_tc_pairs() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(g_tc_mu);
+  auto it = g_tc_pairs.find(dev);
+  return it == g_tc_pairs.end() ? 0 : it->second;
+}
+
+cudaError_t launch_ns_tc(const NsParams& p, cudaStream_t s, int num_sms) {
+  if (p.total_tiles <= 0) return cudaSuccess;
+  cudaError_t e = prepare_ns_tc();
+  if (e != cudaSuccess) return e;
+  if (p.pair) {
+    const int pairs = ns_tc_pairs();
+    if (pairs < 1) return cudaErrorInvalidConfiguration;
+    const int grid = 2 * (p.total_tiles < pairs ? p.total_tiles : pairs);
+    if (p.osq_part && p.last_iter)
+      tc::ns_tc_pair_kernel<true, kPairStages><<<grid, tc::NUM_THREADS, tc::smem_bytes_pair<kPairStages>(), s>>>(p);
+    else
+      tc::ns_tc_pair_kernel<false, kPairStages><<<grid, tc::NUM_THREADS, tc::smem_bytes_pair<kPairStages>(), s>>>(p);
+    return cudaGetLastError();
   }
   const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
   // Three stages for POLY and the first UPDATE: the 48 KB of shared memory they free

@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(TL_NT, sizeof(WT) + sizeof(GT) <= 4 ? 3 : 2) t
             float ss = 0.f;
 #pragma unroll 4
             for (int q = 0; q < T; ++q) ss += __ldcg(mt.part + (size_t)q * B + col);
+            if (p.check_finite) note_nonfinite(p.status, ss);
             const float iv = inv_norm_from_sumsq(ss);
             __stcg(mt.inv + col, iv);
             nonzero = iv > 0.f;
@@ -257,23 +258,33 @@ __global__ void __launch_bounds__(TL_NT, sizeof(WT) + sizeof(GT) <= 4 ? 3 : 2) t
   }
 }
 
+// Resident CTAs per SM of one instantiation on the current device (queried once per
+// device, process-wide).
 template <typename WT, typename GT>
-cudaError_t launch_tall_t(const TallParams& p, int num_sms, cudaStream_t s) {
+cudaError_t tall_resident(int* per_sm) {
   auto kern = tall_kernel<WT, GT>;
   static std::mutex mu;
   static std::map<int, int> resident;   // device -> CTAs per SM
-  int dev = 0, per_sm = 0;
+  int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    auto it = resident.find(dev);
-    if (it == resident.end()) {
-      if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, TL_NT, 0)) != cudaSuccess) return e;
-      it = resident.emplace(dev, per_sm).first;
-    }
-    per_sm = it->second;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = resident.find(dev);
+  if (it == resident.end()) {
+    int n = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, TL_NT, 0)) != cudaSuccess) return e;
+    it = resident.emplace(dev, n).first;
   }
+  *per_sm = it->second;
+  return cudaSuccess;
+}
+
+template <typename WT, typename GT>
+cudaError_t launch_tall_t(const TallParams& p, int num_sms, cudaStream_t s) {
+  auto kern = tall_kernel<WT, GT>;
+  int per_sm = 0;
+  cudaError_t e = tall_resident<WT, GT>(&per_sm);
+  if (e != cudaSuccess) return e;
   long long grid = (long long)num_sms * (per_sm > 0 ? per_sm : 1);
   if (grid > p.total) grid = p.total;
   kern<<<(unsigned)grid, TL_NT, 0, s>>>(p);
@@ -283,6 +294,15 @@ cudaError_t launch_tall_t(const TallParams& p, int num_sms, cudaStream_t s) {
 }  // namespace
 
 int tall_ctrl_words(int nchunks) { return 2 + 2 * nchunks; }
+
+cudaError_t prepare_tall() {
+  int n = 0;
+  cudaError_t e;
+  if ((e = tall_resident<bf16, bf16>(&n)) != cudaSuccess) return e;
+  if ((e = tall_resident<bf16, float>(&n)) != cudaSuccess) return e;
+  if ((e = tall_resident<float, bf16>(&n)) != cudaSuccess) return e;
+  return tall_resident<float, float>(&n);
+}
 
 cudaError_t launch_tall(int w_dt, int g_dt, const TallParams& p, int num_sms, cudaStream_t s) {
   if (p.total <= 0) return cudaSuccess;

@@ -89,3 +89,23 @@ def rel_fro(got, ref):
     ref = np.asarray(ref, dtype=np.float64)
     d = np.linalg.norm(ref)
     return float(np.linalg.norm(got - ref) / d) if d > 0 else float(np.linalg.norm(got))
+
+
+def check_implied_direction(got, prevW, refW_exact, eta, lam, s, tol, what=""):
+    """Newton-Schulz direction implied by a refresh step's stored W:
+        O = (W_prev*(1 - eta*lam) - W_new) / (eta*s),
+    for the GPU's W_new and for the oracle's unrounded W_new.  The GPU's implied O must
+    be within `tol` (relative Frobenius) of the oracle's, plus the storage rounding of
+    W_new: at most half an ulp per element (of bf16 or fp32), divided by eta*s."""
+    got = np.asarray(got, dtype=np.float64)
+    prevW = np.asarray(prevW, dtype=np.float64)
+    refW_exact = np.asarray(refW_exact, dtype=np.float64)
+    keep = prevW * (1.0 - eta * lam)
+    O_got = (keep - got) / (eta * s)
+    O_ref = (keep - refW_exact) / (eta * s)
+    half_ulp = 0.5 * bf16_ulp(np.maximum(np.abs(got), np.abs(refW_exact)))
+    err = np.linalg.norm(O_got - O_ref)
+    lim = tol * np.linalg.norm(O_ref) + np.linalg.norm(half_ulp) / (eta * s)
+    assert err <= lim, f"{what}: implied direction error {err:.3e} > {lim:.3e} " \
+                       f"(relative {err / max(np.linalg.norm(O_ref), 1e-30):.3e})"
+    return err / max(np.linalg.norm(O_ref), 1e-30)

@@ -9,7 +9,8 @@ import torch
 
 from oracle import muon_ref
 from parity_util import (SCALES8, TOL_F32, TOL_NS5_BF16, TOL_NS5_F32, apply_terms, assert_bf16_close,
-                         assert_bf16_within_ulp, assert_f32_close, dev, inputs, rel_fro, to_dev, to_np)
+                         assert_bf16_within_ulp, assert_f32_close, check_implied_direction, dev, inputs, rel_fro,
+                         to_dev, to_np)
 from synth import gradient_np, quantize_np
 
 pytestmark = pytest.mark.gpu
@@ -217,6 +218,31 @@ def test_ns5_parity(mode, tol, steps):
     print(f"ns5 {mode} steps={steps}: " + ", ".join(f"{k[0]}x{k[1]} {v:.2e}" for k, v in worst.items()))
 
 
+@pytest.mark.parametrize("steps", [1, 4])
+def test_ns5_cta_pair_tiles_parity(steps):
+    """The 2-CTA form of the tensor-core GEMMs (tcgen05 cta_group::2 on 256 x 256 tiles,
+    selected by a test hook; the default runs one CTA per 128 x 256 tile) against the
+    oracle: ragged n (300, 520, 130: a pair tile whose second CTA is partly or wholly
+    past the last row), n < 128, tall and wide."""
+    shapes = NS_SHAPES
+    M0 = [mixed_momentum(s, steps, seed=i) for i, s in enumerate(shapes)]
+    M = [to_dev(m, "f32") for m in M0]
+    O = [torch.full(s, 9.0, device=dev(), dtype=torch.bfloat16) for s in shapes]
+    ws = mm.alloc_workspace(shapes)
+    mm.muon_debug_set(mm.MUON_DEBUG_PAIR, 0)
+    try:
+        mm.muon_ns5_batched(M, O, ws)
+    finally:
+        mm.muon_debug_set(0, 0)
+    torch.cuda.synchronize()
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+    for i in range(len(shapes)):
+        err = rel_fro(to_np(O[i]), muon_ref.newton_schulz(M0[i].astype(np.float64)))
+        assert err <= TOL_NS5_BF16, (shapes[i], err)
+        if min(shapes[i]) >= 128:
+            assert err <= 8e-3, (shapes[i], err)
+
+
 def test_ns5_zero_matrix_and_scale_invariance():
     shapes = [(64, 128), (128, 64), (300, 1000)]
     M0 = [np.zeros(shapes[0], np.float32), mixed_momentum(shapes[1], 1), mixed_momentum(shapes[2], 1)]
@@ -258,6 +284,74 @@ def test_refresh_step_parity(dt, mode):
         ulp = 2.0 ** -23 if dt == "f32" else 2.0 ** -7
         round_budget = np.linalg.norm(np.abs(refW)) * ulp
         assert np.linalg.norm(got - refW) <= tol * np.linalg.norm(dW) + round_budget, shapes[i]
+
+
+@pytest.mark.parametrize("eta", [0.02, 1.0])
+def test_refresh_step_bf16_w_implied_direction(eta):
+    """The fused apply of the last UPDATE on bf16 W, checked through the direction it
+    applied: O = (W_prev*(1 - eta*lam) - W_new)/(eta*0.2*sqrt(max(A, B))) against the
+    oracle's NS5 output within the NS5 tolerance plus half a bf16 ulp of W_new per
+    element.  At eta = 1 the update dominates W and the rounding budget is small, so
+    the bound pins O itself.  Shapes cover each store branch of the epilogue: wide rows
+    with 32-byte vectors (256 x 1024), 16-byte vectors (300 x 1000), element stores
+    (520 x 1100, 129 x 129, 33 x 100), and tall matrices stored transposed."""
+    shapes = [(256, 1024), (1024, 256), (300, 1000), (1000, 300), (520, 1100), (1100, 520), (129, 129), (33, 100)]
+    W0, Gs = inputs(shapes, "bf16", "bf16", 1, seed=4)
+    M0 = [mixed_momentum(s, 3, seed=20 + i) for i, s in enumerate(shapes)]
+    W = [to_dev(w, "bf16") for w in W0]
+    M = [to_dev(m, "f32") for m in M0]
+    G = [to_dev(g, "bf16") for g in Gs[0]]
+    ws = mm.alloc_workspace(shapes)
+    assert mm.muon_periodic_step(W, G, M, 0, ws, K=3, eta=eta) == mm.MUON_BRANCH_NS5
+    torch.cuda.synchronize()
+    errs = {}
+    for i, (a, b) in enumerate(shapes):
+        refW64, refM, _ = muon_ref.periodic_step(W0[i], M0[i], Gs[0][i], 0, 3, 0.15, 0.95, eta, 0.01, w_dtype="f64")
+        assert_f32_close(to_np(M[i]), refM, what=f"M {shapes[i]}")
+        s = muon_ref.update_scale(a, b, True, 0.15)
+        errs[shapes[i]] = check_implied_direction(to_np(W[i]), W0[i], refW64, eta, 0.01, s, TOL_NS5_BF16,
+                                                  what=str(shapes[i]))
+    print(f"eta={eta}: " + ", ".join(f"{k[0]}x{k[1]} {v:.2e}" for k, v in errs.items()))
+
+
+# Shape groups (same short and long side) beyond the 8 one Newton-Schulz launch
+# takes, and a group beyond the 512 matrices of one launch table.
+MANY_GROUP_SHAPES = [(32, 64), (48, 80), (64, 96), (72, 200), (96, 96), (100, 300), (300, 100), (130, 260),
+                     (128, 512), (200, 330), (256, 384), (40, 1000)] + [(8, 16)] * 515 + [(16, 8)] * 5
+
+
+def test_ns5_more_groups_and_matrices_than_one_launch_takes():
+    shapes = MANY_GROUP_SHAPES
+    M0 = [mixed_momentum(s, 2, seed=i) for i, s in enumerate(shapes)]
+    M = [to_dev(m, "f32") for m in M0]
+    O = [torch.full(s, 9.0, device=dev(), dtype=torch.bfloat16) for s in shapes]
+    ws = mm.alloc_workspace(shapes)
+    mm.muon_ns5_batched(M, O, ws)
+    torch.cuda.synchronize()
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+    for i, s in enumerate(shapes):
+        err = rel_fro(to_np(O[i]), muon_ref.newton_schulz(M0[i].astype(np.float64)))
+        assert err <= TOL_NS5_BF16, (i, s, err)
+
+
+@pytest.mark.parametrize("mode", ["bf16", "f32"])
+def test_refresh_step_more_groups_and_matrices_than_one_launch_takes(mode):
+    shapes = MANY_GROUP_SHAPES
+    W0, Gs = inputs(shapes, "f32", "f32", 1, seed=7)
+    M0 = [mixed_momentum(s, 2, seed=100 + i) for i, s in enumerate(shapes)]
+    W = [to_dev(w, "f32") for w in W0]
+    M = [to_dev(m, "f32") for m in M0]
+    G = [to_dev(g, "f32") for g in Gs[0]]
+    ws = mm.alloc_workspace(shapes, mode)
+    assert mm.muon_periodic_step(W, G, M, 3, ws, K=3, ns5_mode=mode) == mm.MUON_BRANCH_NS5
+    torch.cuda.synchronize()
+    assert mm.muon_check_status(ws) == mm.MUON_OK
+    tol = TOL_NS5_BF16 if mode == "bf16" else TOL_NS5_F32
+    for i, (a, b) in enumerate(shapes):
+        refW64, refM, _ = muon_ref.periodic_step(W0[i], M0[i], Gs[0][i], 3, 3, 0.15, 0.95, 0.02, 0.01, w_dtype="f64")
+        assert_f32_close(to_np(M[i]), refM, what=f"M {i} {shapes[i]}")
+        check_implied_direction(to_np(W[i]), W0[i], refW64, 0.02, 0.01, muon_ref.update_scale(a, b, True, 0.15),
+                                tol, what=f"{i} {shapes[i]}")
 
 
 # ---------------------------------------------------------------------------
@@ -384,19 +478,28 @@ def test_misaligned_views_take_the_scalar_path():
 # ---------------------------------------------------------------------------
 # device-side bounded waits: an expired wait is reported, the context survives
 # ---------------------------------------------------------------------------
-def test_stalled_producer_times_out_and_context_survives():
+@pytest.mark.parametrize("pair", [0, 1])
+def test_stalled_producer_times_out_and_context_survives(pair):
+    """The load warp(s) issue nothing: every consumer's bounded wait expires (in the
+    2-CTA form, on both CTAs of each pair), the status reads MUON_ERR_TIMEOUT, and the
+    next call on the same context is exact."""
     shapes = [(256, 512)]
     M = [to_dev(mixed_momentum(shapes[0], 1), "f32")]
     O = [torch.empty(shapes[0], device=dev(), dtype=torch.bfloat16)]
     ws = mm.alloc_workspace(shapes)
-    mm.muon_debug_set(mm.MUON_DEBUG_STALL_PRODUCER, 50)
+    flags = mm.MUON_DEBUG_PAIR if pair else 0
+    mm.muon_debug_set(mm.MUON_DEBUG_STALL_PRODUCER | flags, 50)
     try:
         mm.muon_ns5_batched(M, O, ws)
         assert mm.muon_check_status(ws) == mm.MUON_ERR_TIMEOUT
     finally:
         mm.muon_debug_set(0, 0)
     # the status word was cleared and the context still works
-    mm.muon_ns5_batched(M, O, ws)
+    mm.muon_debug_set(flags, 0)
+    try:
+        mm.muon_ns5_batched(M, O, ws)
+    finally:
+        mm.muon_debug_set(0, 0)
     assert mm.muon_check_status(ws) == mm.MUON_OK
     ref = muon_ref.newton_schulz(to_np(M[0]))
     assert rel_fro(to_np(O[0]), ref) <= TOL_NS5_BF16
