@@ -285,14 +285,14 @@ int muon_abi_version(void);
  * through the single-pass thread-block-cluster kernel (to test every path).
  * MUON_DEBUG_NO_OVERLAP runs the wide-row and tall-column kernels of a RowNorm
  * step one after the other on the caller's stream instead of side by side.
- * MUON_DEBUG_PAIR runs the tensor-core Newton-Schulz GEMMs as 2-CTA clusters
- * (tcgen05 cta_group::2) on 256 x 256 tiles instead of one CTA per 128 x 256 tile. */
+ * MUON_DEBUG_NO_PAIR runs the tensor-core Newton-Schulz GEMMs with one CTA per
+ * 128 x 256 tile instead of 2-CTA clusters (tcgen05 cta_group::2) on 256 x 256 tiles. */
 enum {
   MUON_DEBUG_STALL_PRODUCER = 1,
   MUON_DEBUG_NO_CLUSTER = 2,
   MUON_DEBUG_NO_OVERLAP = 4,
   MUON_DEBUG_TALL_CLUSTER = 8,
-  MUON_DEBUG_PAIR = 16
+  MUON_DEBUG_NO_PAIR = 16
 };
 int muon_debug_set(int flags, int timeout_ms);
 

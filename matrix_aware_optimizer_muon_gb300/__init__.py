@@ -3,7 +3,7 @@
 The compute runs in libmuon_gb300.so (hand-written CUDA); this package is its
 ctypes binding plus a small stateful wrapper.  See include/muon.h for the C ABI.
 """
-from ._lib import (MUON_BRANCH_NS5, MUON_BRANCH_ROWNORM, MUON_DEBUG_NO_CLUSTER, MUON_DEBUG_NO_OVERLAP, MUON_DEBUG_TALL_CLUSTER, MUON_DEBUG_PAIR, MUON_DEBUG_STALL_PRODUCER, MUON_DTYPE_BF16,
+from ._lib import (MUON_BRANCH_NS5, MUON_BRANCH_ROWNORM, MUON_DEBUG_NO_CLUSTER, MUON_DEBUG_NO_OVERLAP, MUON_DEBUG_TALL_CLUSTER, MUON_DEBUG_NO_PAIR, MUON_DEBUG_STALL_PRODUCER, MUON_DTYPE_BF16,
                    MUON_DTYPE_F32, MUON_ERR_CUDA, MUON_ERR_INVALID, MUON_ERR_NO_DEVICE, MUON_ERR_NONFINITE, MUON_ERR_TIMEOUT,
                    MUON_ERR_UNSUPPORTED, MUON_ERR_WORKSPACE, MUON_NS5_BF16, MUON_NS5_F32, MUON_OK, MUON_SCALE_ADJUSTED_LR, MUON_SCALE_UPDATE_NORM, MuonError,
                    MuonMatrix, alloc_workspace, load_library, make_matrices, muon_apply, muon_check_status,

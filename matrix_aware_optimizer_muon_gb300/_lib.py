@@ -36,7 +36,7 @@ MUON_DEBUG_STALL_PRODUCER = 1
 MUON_DEBUG_NO_CLUSTER = 2
 MUON_DEBUG_NO_OVERLAP = 4
 MUON_DEBUG_TALL_CLUSTER = 8
-MUON_DEBUG_PAIR = 16
+MUON_DEBUG_NO_PAIR = 16
 
 _NS5_MODES = {"bf16": MUON_NS5_BF16, "f32": MUON_NS5_F32}
 

@@ -399,11 +399,9 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
   std::vector<int> gbase(ng + 1, 0);
   for (int gi = 0; gi < ng; ++gi) gbase[gi + 1] = gbase[gi] + P.groups[gi].count;
   const float* inv_norm_all = reinterpret_cast<const float*>(ws + P.inv_norm);
-  // Tensor-core launches: one CTA per 128 x 256 tile, or 2-CTA clusters on 256 x 256
-  // tiles (MUON_DEBUG_PAIR).  Under the power cap of a long refresh the pair form
-  // draws the clock lower than it gains per clock (15B set: 210.7 -> 233.7 ms per
-  // step at 1680 -> 1367 MHz; 1.3B set: 11.86 -> 11.65 ms).
-  const bool pair = tcmode && (g_debug_flags.load() & MUON_DEBUG_PAIR);
+  // Tensor-core launches run as 2-CTA clusters on 256 x 256 tiles (tcgen05 cta_group::2),
+  // or with one CTA per 128 x 256 tile under the test hook MUON_DEBUG_NO_PAIR.
+  const bool pair = tcmode && !(g_debug_flags.load() & MUON_DEBUG_NO_PAIR);
   // O^2 partials per tile: one per epilogue warp (of both CTAs of a pair), or one per CTA
   const int slots = tcmode ? (pair ? 16 : 8) : 1;
   long long osq_off = 0;
@@ -524,7 +522,9 @@ int run_ns5(const Plan& P, const muon_matrix* mats, uint8_t* ws, int dst_mode, i
                                                    ((a.cols % 4 == 0 && aligned(a.M, 16)) ? NS_MVEC : 0) |
                                                    ((a.cols % 8 == 0 && aligned(a.M, 32)) ? NS_MVEC8 : 0) |
                                                    ((a.rows <= a.cols && a.cols % 8 == 0 && aligned(dptr, 16)) ? NS_WVEC : 0) |
-                                                   ((a.rows <= a.cols && a.cols % 16 == 0 && aligned(dptr, 32)) ? NS_WVEC8 : 0));
+                                                   ((a.rows <= a.cols && a.cols % 16 == 0 && aligned(dptr, 32)) ? NS_WVEC8 : 0) |
+                                                   ((a.rows > a.cols && a.cols % 4 == 0 && aligned(a.M, 16)) ? NS_MTALL16 : 0) |
+                                                   ((a.rows > a.cols && a.cols % 8 == 0 && aligned(dptr, 16)) ? NS_WTALL16 : 0));
           }
           mbase += g.count;
         }

@@ -246,7 +246,11 @@ struct LineFinalParams {
 enum GemmKind : int { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_UPDATE = 2 };
 // NS_MVEC / NS_WVEC: M rows / the destination's rows take 16-byte vectors; the
 // ...8 forms: 32-byte vectors (256-bit accesses, 32-byte aligned rows).
-enum NsFlags : int { NS_TALL = 1, NS_MVEC = 2, NS_WVEC = 4, NS_MVEC8 = 8, NS_WVEC8 = 16 };
+// NS_MTALL16 / NS_WTALL16: a tall matrix whose M / W rows start 16-byte aligned (n a
+// multiple of 4 / 8 elements and an aligned base), so the epilogue can fetch 32 of
+// its short-side elements with one bulk copy.
+enum NsFlags : int { NS_TALL = 1, NS_MVEC = 2, NS_WVEC = 4, NS_MVEC8 = 8, NS_WVEC8 = 16, NS_MTALL16 = 32,
+                     NS_WTALL16 = 64 };
 // Iterations 1..NS_LO_ITERS add a*X_lo, the bf16 residual of X, to (B + aI) X_hi
 // (X carried with ~16 significant bits where the small singular directions are
 // still far below the element magnitudes).

@@ -47,9 +47,12 @@ constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int EPI_CHUNKS = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per epilogue warp
 constexpr uint32_t TMEM_COLS = 512;
-template <int kStages>
-constexpr int smem_bytes() { return kStages * STAGE_BYTES + 1024 + 256; }
-constexpr int SMEM_BYTES = smem_bytes<STAGES>();
+constexpr int BAR_BYTES = 256;   // mbarriers, the TMEM address and the abort flag
+constexpr int SMEM_LIMIT = 227 * 1024;
+// Dynamic shared memory of a launch: the operand ring, the 1 KB alignment slack of the
+// swizzled ring, the barriers.
+constexpr int smem_bytes(int stage_bytes, int stages) { return stages * stage_bytes + 1024 + BAR_BYTES; }
+constexpr int SMEM_BYTES = smem_bytes(STAGE_BYTES, STAGES);
 
 struct Tile {
   int g, mat, tm, tn;
@@ -391,6 +394,96 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
   }
 }
 
+constexpr int P_A_BYTES = BM * BK * 2;            // this CTA's 128 rows of A
+constexpr int P_B_BYTES = (BN / 2) * BK * 2;      // this CTA's 128 columns of B
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+
+
+// Pair tiles: G.mtiles counts 256-row blocks.  ti.tm is this CTA's 128-row block.
+__device__ __forceinline__ Tile decode_pair(const NsParams& p, int t, int rank) {
+  Tile ti;
+  int g = 0;
+  while (g + 1 < p.ngroups && p.g[g + 1].tile_begin <= t) ++g;
+  const NsGroup& G = p.g[g];
+  const int lt = t - G.tile_begin;
+  ti.g = g;
+  ti.mat = lt / G.tiles_per_mat;
+  int r = lt - ti.mat * G.tiles_per_mat;
+  int tp;
+  if (p.kind == GEMM_UPDATE) {
+    ti.tn = r / G.mtiles;
+    tp = r - ti.tn * G.mtiles;
+  } else {
+    // upper-triangle 256 x 256 tiles: column block tn holds row blocks 0 .. tn
+    int tn = 0;
+    while (true) {
+      const int cnt = min(tn + 1, G.mtiles);
+      if (r < cnt) break;
+      r -= cnt;
+      ++tn;
+    }
+    ti.tn = tn;
+    tp = r;
+  }
+  ti.tm = 2 * tp + rank;
+  return ti;
+}
+
+// Epilogue warps of either kernel form: drain each tile's accumulator, combine it with
+// the chunk inputs, store.  kPairMode: tiles are 256 x 256 pair tiles walked by
+// cluster, tile rows are this CTA's half, and the accumulator-empty barrier lives in
+// the even CTA.
+template <bool kOsq, bool kPairMode>
+__device__ __forceinline__ void epilogue_loop(const NsParams& p, int t0, int tstride, int rank, int warp, int lane,
+                                              uint32_t tmem_base, uint64_t* tfull, uint64_t* tempty,
+                                              volatile int* abort_flag) {
+  const int quarter = warp & 3;            // TMEM lanes this warp may access
+  const int half = (warp - 2) >> 2;        // which half of the 256 columns it drains
+  const int row_in_tile = quarter * 32 + lane;
+  const int ew = warp - 2;
+  int it = 0;
+  for (int t = t0; t < p.total_tiles; t += tstride, ++it) {
+    const Tile ti = kPairMode ? decode_pair(p, t, rank) : decode(p, t);
+    const NsGroup& G = p.g[ti.g];
+    const int acc = it & 1;
+    const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+    const int r = ti.tm * BM + row_in_tile;
+    const int cbase = ti.tn * BN + half * (EPI_CHUNKS * 32);
+    ChunkIn in_a, in_b;
+    float osq = 0.f;
+    epi_prefetch(p, G, ti, r, cbase, in_a);   // does not depend on this tile's accumulator
+    int ok = 1;
+    if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, p, true) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    ptx::tc_fence_after();
+    const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * EPI_CHUNKS * 32);
+#pragma unroll
+    for (int k = 0; k < EPI_CHUNKS; ++k) {
+      const int c0 = cbase + k * 32;
+      ChunkIn& cur = (k & 1) ? in_b : in_a;
+      ChunkIn& nxt = (k & 1) ? in_a : in_b;
+      float v[32];
+      ptx::tmem_ld_32x32b_x32(tbase + k * 32, v);
+      if (k + 1 < EPI_CHUNKS) epi_prefetch(p, G, ti, r, c0 + 32, nxt);
+      epi_finish<kOsq>(p, G, ti, r, c0, v, cur, osq);
+    }
+    if (kOsq && p.last_iter) {   // one fixed slot per (tile, CTA, epilogue warp)
+      osq = warp_sum(osq);
+      if (lane == 0) {
+        const size_t slot_i = kPairMode ? ((size_t)t * 2 + rank) * NUM_EPI_WARPS + ew : (size_t)t * NUM_EPI_WARPS + ew;
+        p.osq_part[slot_i] = osq;
+      }
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (!kPairMode || rank == 0) ptx::mbar_arrive(&tempty[acc]);
+      else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_addr(&tempty[acc]), 0));
+    }
+  }
+}
+
 // kOsq: the last UPDATE also writes per-warp partial sums of O^2 (only launches
 // that need them pay for them).  kStages: depth of the TMA/MMA ring.
 template <bool kOsq, int kStages>
@@ -517,41 +610,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;            // TMEM lanes this warp may access
-    const int half = (warp - 2) >> 2;        // which half of the 256 columns it drains
-    const int row_in_tile = quarter * 32 + lane;
-    int it = 0;
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
-      const Tile ti = decode(p, t);
-      const NsGroup& G = p.g[ti.g];
-      const int acc = it & 1;
-      const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-      const int r = ti.tm * BM + row_in_tile;
-      const int cbase = ti.tn * BN + half * (EPI_CHUNKS * 32);
-      ChunkIn in[2];
-      float osq = 0.f;
-      epi_prefetch(p, G, ti, r, cbase, in[0]);   // does not depend on this tile's accumulator
-      int ok = 1;
-      if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, p, true) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * EPI_CHUNKS * 32);
-#pragma unroll
-      for (int k = 0; k < EPI_CHUNKS; ++k) {
-        float v[32];
-        ptx::tmem_ld_32x32b_x32(tbase + k * 32, v);
-        if (k + 1 < EPI_CHUNKS) epi_prefetch(p, G, ti, r, cbase + (k + 1) * 32, in[(k + 1) & 1]);
-        epi_finish<kOsq>(p, G, ti, r, cbase + k * 32, v, in[k & 1], osq);
-      }
-      if (kOsq && p.last_iter) {   // one fixed slot per (tile, epilogue warp)
-        osq = warp_sum(osq);
-        if (lane == 0) p.osq_part[(size_t)t * NUM_EPI_WARPS + (warp - 2)] = osq;
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
-    }
+    epilogue_loop<kOsq, false>(p, blockIdx.x, gridDim.x, 0, warp, lane, tmem_base, tfull, tempty, abort_flag);
   }
 
   ptx::tc_fence_before();
@@ -573,42 +632,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
 //   tfull[a]  (both CTAs): the tile's last commit, multicast;
 //   tempty[a] (even CTA): the 16 epilogue warps of both CTAs arrive on it.
 // ---------------------------------------------------------------------------
-constexpr int P_A_BYTES = BM * BK * 2;            // this CTA's 128 rows of A
-constexpr int P_B_BYTES = (BN / 2) * BK * 2;      // this CTA's 128 columns of B
-constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-template <int kStages>
-constexpr int smem_bytes_pair() { return kStages * P_STAGE_BYTES + 1024 + 256; }
-
-// Pair tiles: G.mtiles counts 256-row blocks.  ti.tm is this CTA's 128-row block.
-__device__ __forceinline__ Tile decode_pair(const NsParams& p, int t, int rank) {
-  Tile ti;
-  int g = 0;
-  while (g + 1 < p.ngroups && p.g[g + 1].tile_begin <= t) ++g;
-  const NsGroup& G = p.g[g];
-  const int lt = t - G.tile_begin;
-  ti.g = g;
-  ti.mat = lt / G.tiles_per_mat;
-  int r = lt - ti.mat * G.tiles_per_mat;
-  int tp;
-  if (p.kind == GEMM_UPDATE) {
-    ti.tn = r / G.mtiles;
-    tp = r - ti.tn * G.mtiles;
-  } else {
-    // upper-triangle 256 x 256 tiles: column block tn holds row blocks 0 .. tn
-    int tn = 0;
-    while (true) {
-      const int cnt = min(tn + 1, G.mtiles);
-      if (r < cnt) break;
-      r -= cnt;
-      ++tn;
-    }
-    ti.tn = tn;
-    tp = r;
-  }
-  ti.tm = 2 * tp + rank;
-  return ti;
-}
-
 template <bool kOsq, int kStages>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ns_tc_pair_kernel(const __grid_constant__ NsParams p) {
@@ -739,44 +762,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int row_in_tile = quarter * 32 + lane;
-    int it = 0;
-    for (int t = pair; t < p.total_tiles; t += npairs, ++it) {
-      const Tile ti = decode_pair(p, t, rank);
-      const NsGroup& G = p.g[ti.g];
-      const int acc = it & 1;
-      const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-      const int r = ti.tm * BM + row_in_tile;
-      const int cbase = ti.tn * BN + half * (EPI_CHUNKS * 32);
-      ChunkIn in[2];
-      float osq = 0.f;
-      epi_prefetch(p, G, ti, r, cbase, in[0]);
-      int ok = 1;
-      if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, p, true) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * EPI_CHUNKS * 32);
-#pragma unroll
-      for (int k = 0; k < EPI_CHUNKS; ++k) {
-        float v[32];
-        ptx::tmem_ld_32x32b_x32(tbase + k * 32, v);
-        if (k + 1 < EPI_CHUNKS) epi_prefetch(p, G, ti, r, cbase + (k + 1) * 32, in[(k + 1) & 1]);
-        epi_finish<kOsq>(p, G, ti, r, cbase + k * 32, v, in[k & 1], osq);
-      }
-      if (kOsq && p.last_iter) {   // one fixed slot per (pair tile, CTA, epilogue warp)
-        osq = warp_sum(osq);
-        if (lane == 0) p.osq_part[((size_t)t * 2 + rank) * NUM_EPI_WARPS + (warp - 2)] = osq;
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (even) ptx::mbar_arrive(&tempty[acc]);
-        else ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_addr(&tempty[acc]), 0));
-      }
-    }
+    epilogue_loop<kOsq, true>(p, pair, npairs, rank, warp, lane, tmem_base, tfull, tempty, abort_flag);
   }
 
   ptx::tc_fence_before();
@@ -795,10 +781,36 @@ int ns_tc_smem_bytes() { return tc::SMEM_BYTES; }
 namespace {
 std::mutex g_tc_mu;
 std::map<int, int> g_tc_pairs;   // device -> co-resident 2-CTA clusters
-#ifndef MUON_PAIR_STAGES
-#define MUON_PAIR_STAGES 6
+// Ring depth of the 2-CTA form (32 KB a stage), for launches whose epilogue reads no
+// global input (the Gram products, the UPDATE of iteration 3) and for the others.
+// Four stages hold as many K steps in flight as the one-CTA form's four, in 128 KB
+// instead of 192, and leave L1 room for the row-per-lane epilogue loads.  Measured
+// (step ms, 15B / 1.3B; MMA-EPI stages): 4-4 205.6 / 11.35, 6-4 208.1 / 11.25,
+// 6-5 215.1 / 11.18, 6-3 222.9 / 11.77; the one-CTA form 205.8 / 11.68.  Deeper
+// rings lose at 15B, where the step runs under the power cap.
+#ifndef MUON_PAIR_STAGES_MMA
+#define MUON_PAIR_STAGES_MMA 4
 #endif
-constexpr int kPairStages = MUON_PAIR_STAGES;
+#ifndef MUON_PAIR_STAGES_EPI
+#define MUON_PAIR_STAGES_EPI 4
+#endif
+constexpr int kPairMma = MUON_PAIR_STAGES_MMA, kPairEpi = MUON_PAIR_STAGES_EPI;
+
+template <class K>
+cudaError_t allow_smem(K kern) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_LIMIT);
+}
+
+// Whether a launch's epilogue reads global inputs: POLY (S), the first UPDATE (fp32
+// M), the UPDATEs that carry X's residual, and the last UPDATE when it applies to W.
+bool reads_epilogue_inputs(const NsParams& p) {
+  if (p.kind == GEMM_POLY) return true;
+  if (p.kind != GEMM_UPDATE) return false;
+  if (p.first_iter) return true;
+  for (int g = 0; g < p.ngroups; ++g)
+    if (p.g[g].lo_in) return true;
+  return p.last_iter && p.dst_mode == 1;
+}
 }  // namespace
 
 cudaError_t prepare_ns_tc() {
@@ -807,27 +819,19 @@ cudaError_t prepare_ns_tc() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_tc_mu);
   if (g_tc_pairs.count(dev)) return cudaSuccess;
-  e = cudaFuncSetAttribute(tc::ns_tc_kernel<false, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           tc::smem_bytes<4>());
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc::ns_tc_kernel<false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           tc::smem_bytes<3>());
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc::ns_tc_kernel<true, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           tc::smem_bytes<4>());
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc::ns_tc_pair_kernel<false, kPairStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           tc::smem_bytes_pair<kPairStages>());
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc::ns_tc_pair_kernel<true, kPairStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           tc::smem_bytes_pair<kPairStages>());
-  if (e != cudaSuccess) return e;
+  if ((e = allow_smem(tc::ns_tc_kernel<false, 4>)) != cudaSuccess) return e;
+  if ((e = allow_smem(tc::ns_tc_kernel<false, 3>)) != cudaSuccess) return e;
+  if ((e = allow_smem(tc::ns_tc_kernel<true, 4>)) != cudaSuccess) return e;
+  if ((e = allow_smem(tc::ns_tc_pair_kernel<false, kPairMma>)) != cudaSuccess) return e;
+  if ((e = allow_smem(tc::ns_tc_pair_kernel<false, kPairEpi>)) != cudaSuccess) return e;
+  if ((e = allow_smem(tc::ns_tc_pair_kernel<true, kPairMma>)) != cudaSuccess) return e;
+  if ((e = allow_smem(tc::ns_tc_pair_kernel<true, kPairEpi>)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(tc::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = tc::smem_bytes_pair<kPairStages>();
+  cfg.dynamicSmemBytes = tc::smem_bytes(tc::P_STAGE_BYTES, kPairMma > kPairEpi ? kPairMma : kPairEpi);
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, tc::ns_tc_pair_kernel<false, kPairStages>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, tc::ns_tc_pair_kernel<false, kPairMma>, &cfg);
   if (e != cudaSuccess) return e;
   g_tc_pairs[dev] = clusters;
   return cudaSuccess;
@@ -845,29 +849,36 @@ cudaError_t launch_ns_tc(const NsParams& p, cudaStream_t s, int num_sms) {
   if (p.total_tiles <= 0) return cudaSuccess;
   cudaError_t e = prepare_ns_tc();
   if (e != cudaSuccess) return e;
+  const bool osq = p.osq_part && p.last_iter;
+  const bool inputs = reads_epilogue_inputs(p);
   if (p.pair) {
     const int pairs = ns_tc_pairs();
     if (pairs < 1) return cudaErrorInvalidConfiguration;
     const int grid = 2 * (p.total_tiles < pairs ? p.total_tiles : pairs);
-    if (p.osq_part && p.last_iter)
-      tc::ns_tc_pair_kernel<true, kPairStages><<<grid, tc::NUM_THREADS, tc::smem_bytes_pair<kPairStages>(), s>>>(p);
+    const int smem = tc::smem_bytes(tc::P_STAGE_BYTES, inputs ? kPairEpi : kPairMma);
+    if (osq && inputs)
+      tc::ns_tc_pair_kernel<true, kPairEpi><<<grid, tc::NUM_THREADS, smem, s>>>(p);
+    else if (osq)
+      tc::ns_tc_pair_kernel<true, kPairMma><<<grid, tc::NUM_THREADS, smem, s>>>(p);
+    else if (inputs)
+      tc::ns_tc_pair_kernel<false, kPairEpi><<<grid, tc::NUM_THREADS, smem, s>>>(p);
     else
-      tc::ns_tc_pair_kernel<false, kPairStages><<<grid, tc::NUM_THREADS, tc::smem_bytes_pair<kPairStages>(), s>>>(p);
+      tc::ns_tc_pair_kernel<false, kPairMma><<<grid, tc::NUM_THREADS, smem, s>>>(p);
     return cudaGetLastError();
   }
   const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
-  // Three stages for POLY and the first UPDATE: the 48 KB of shared memory they free
-  // go to L1, where those launches' epilogue loads gain more than a shallower ring
-  // costs them (per launch on the 1.3B set: POLY 655 -> 584 us, UPDATE 0 4371 -> 4024
-  // us; the long-K Gram product and the later UPDATEs lose 14-15% with three).
-  const bool three = !(p.osq_part && p.last_iter) &&
-                     (p.kind == GEMM_POLY || (p.kind == GEMM_UPDATE && p.first_iter));
-  if (p.osq_part && p.last_iter)
-    tc::ns_tc_kernel<true, 4><<<grid, tc::NUM_THREADS, tc::smem_bytes<4>(), s>>>(p);
+  // One-CTA form, 48 KB a stage.  Three stages for POLY and the first UPDATE: the 48 KB
+  // they free go to L1, where those launches' epilogue loads gain more than a shallower
+  // ring costs them (per launch on the 1.3B set: POLY 655 -> 584 us, UPDATE 0 4371 ->
+  // 4024 us; the long-K Gram product and the later UPDATEs lose 14-15% with three).
+  const bool three = !osq && (p.kind == GEMM_POLY || (p.kind == GEMM_UPDATE && p.first_iter));
+  const int smem = tc::smem_bytes(tc::STAGE_BYTES, three ? 3 : 4);
+  if (osq)
+    tc::ns_tc_kernel<true, 4><<<grid, tc::NUM_THREADS, smem, s>>>(p);
   else if (three)
-    tc::ns_tc_kernel<false, 3><<<grid, tc::NUM_THREADS, tc::smem_bytes<3>(), s>>>(p);
+    tc::ns_tc_kernel<false, 3><<<grid, tc::NUM_THREADS, smem, s>>>(p);
   else
-    tc::ns_tc_kernel<false, 4><<<grid, tc::NUM_THREADS, tc::smem_bytes<4>(), s>>>(p);
+    tc::ns_tc_kernel<false, 4><<<grid, tc::NUM_THREADS, smem, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -22,7 +22,7 @@ the pages, in the pages' order and notation:
   (the distributed-implementation paragraph: "tall matrices only all-reduce the
   per-column norm scalars").
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 * the RowNorm lines are the min(A, B) lines along the long dimension: rows when
   A <= B (square counts as wide), columns when A > B;
 * RowNorm steps use the scale gamma*0.2*sqrt(max(A, B)); weight decay applies on

@@ -219,17 +219,18 @@ def test_ns5_parity(mode, tol, steps):
 
 
 @pytest.mark.parametrize("steps", [1, 4])
-def test_ns5_cta_pair_tiles_parity(steps):
-    """The 2-CTA form of the tensor-core GEMMs (tcgen05 cta_group::2 on 256 x 256 tiles,
-    selected by a test hook; the default runs one CTA per 128 x 256 tile) against the
-    oracle: ragged n (300, 520, 130: a pair tile whose second CTA is partly or wholly
-    past the last row), n < 128, tall and wide."""
+def test_ns5_one_cta_tiles_parity(steps):
+    """The one-CTA form of the tensor-core GEMMs (128 x 256 tiles, selected by a test
+    hook; the default runs 2-CTA clusters with tcgen05 cta_group::2 on 256 x 256 tiles)
+    against the oracle, on the shapes of the default-form test above: ragged n (300,
+    520, 130: a pair tile whose second CTA is partly or wholly past the last row), n <
+    128, tall and wide."""
     shapes = NS_SHAPES
     M0 = [mixed_momentum(s, steps, seed=i) for i, s in enumerate(shapes)]
     M = [to_dev(m, "f32") for m in M0]
     O = [torch.full(s, 9.0, device=dev(), dtype=torch.bfloat16) for s in shapes]
     ws = mm.alloc_workspace(shapes)
-    mm.muon_debug_set(mm.MUON_DEBUG_PAIR, 0)
+    mm.muon_debug_set(mm.MUON_DEBUG_NO_PAIR, 0)
     try:
         mm.muon_ns5_batched(M, O, ws)
     finally:
@@ -487,7 +488,7 @@ def test_stalled_producer_times_out_and_context_survives(pair):
     M = [to_dev(mixed_momentum(shapes[0], 1), "f32")]
     O = [torch.empty(shapes[0], device=dev(), dtype=torch.bfloat16)]
     ws = mm.alloc_workspace(shapes)
-    flags = mm.MUON_DEBUG_PAIR if pair else 0
+    flags = 0 if pair else mm.MUON_DEBUG_NO_PAIR
     mm.muon_debug_set(mm.MUON_DEBUG_STALL_PRODUCER | flags, 50)
     try:
         mm.muon_ns5_batched(M, O, ws)
