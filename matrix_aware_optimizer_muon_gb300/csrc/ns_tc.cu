@@ -12,19 +12,22 @@
 // a separate pass.  In the last iteration the UPDATE epilogue either writes O or
 // applies W <- W - eta*(0.2*sqrt(max(A, B))*O + lambda*W) (Eq. (4)/(7)) directly.
 //
-// Kernel shape: persistent, one CTA per SM, 320 threads.
-//   warp 0      TMA producer (one lane): 4-stage ring (3 for POLY and the first
-//               UPDATE) of 128x64 A and 256x64 B
-//               bf16 tiles, 128-byte swizzle;
-//   warp 1      TMEM allocator and MMA issuer (one lane): tcgen05.mma
-//               cta_group::1, M=128, N=256, K=16, two 256-column fp32
-//               accumulators so the epilogue of tile i overlaps the MMAs of i+1;
+// Two kernel forms share the roles and the epilogue:
+//   ns_tc_pair_kernel (default): 2-CTA clusters (tcgen05 cta_group::2) on 256 x 256
+//               tiles, each CTA staging half of A and half of B (32 KB a K step);
+//   ns_tc_kernel: one CTA per 128 x 256 tile (48 KB a K step).
+// Both are persistent (one CTA per SM), 320 threads:
+//   warp 0      TMA producer (one lane): mbarrier ring of A and B tiles, 128-byte
+//               swizzle;
+//   warp 1      TMEM allocator and MMA issuer (one lane; in the pair form only the
+//               even CTA issues): tcgen05.mma kind::f16, K = 16, two 256-column
+//               fp32 accumulators so the epilogue of tile i overlaps the MMAs of i+1;
 //   warps 2..9  epilogue, two per TMEM lane quarter, each draining 128 of the
 //               256 columns: tcgen05.ld of the accumulator rows, fused combine,
 //               global stores (symmetric outputs are written with their mirror).
 // Tiles of all same-shape matrices (and of several shape groups) form one flat
-// list that CTAs walk with stride gridDim.x.  Every mbarrier wait is bounded in
-// time; on expiry the kernel records MUON_DEV_TIMEOUT in the status word, all
+// list that CTAs (or clusters) walk with a stride.  Every mbarrier wait is bounded
+// in time; on expiry the kernel records MUON_DEV_TIMEOUT in the status word, all
 // roles stop, in-flight copies and MMAs are drained (again bounded) and TMEM is
 // freed before exit.
 #include <map>
@@ -394,6 +397,19 @@ __device__ __forceinline__ void epi_finish(const NsParams& p, const NsGroup& G, 
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair form (tcgen05 cta_group::2): a 2-CTA cluster computes a 256 x 256 output
+// tile.  The even CTA issues every MMA (M = 256, N = 256, K = 16); each CTA stages
+// its own 128 rows of A and 128 columns (N) of B per K step, 32 KB a stage instead
+// of 48, so four stages hold as many K steps in flight as the one-CTA form's four in
+// two thirds of the shared memory, and each CTA's tensor memory receives its 128 rows of the tile, drained by its own
+// epilogue warps exactly as in the one-CTA form.
+//   full[s]   (even CTA): the producers of both CTAs land their halves on it; the
+//             even producer posts the expected bytes of both;
+//   empty[s]  (both CTAs): the MMA commit arrives on both, multicast;
+//   tfull[a]  (both CTAs): the tile's last commit, multicast;
+//   tempty[a] (even CTA): the 16 epilogue warps of both CTAs arrive on it.
+// ---------------------------------------------------------------------------
 constexpr int P_A_BYTES = BM * BK * 2;            // this CTA's 128 rows of A
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;      // this CTA's 128 columns of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
@@ -619,19 +635,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
   if (warp == 1) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
-// ---------------------------------------------------------------------------
-// CTA-pair form (tcgen05 cta_group::2): a 2-CTA cluster computes a 256 x 256 output
-// tile.  The even CTA issues every MMA (M = 256, N = 256, K = 16); each CTA stages
-// its own 128 rows of A and 128 columns (N) of B per K step, 32 KB a stage instead
-// of 48, so the same shared memory holds half again as many K steps in flight, and
-// each CTA's tensor memory receives its 128 rows of the tile, drained by its own
-// epilogue warps exactly as in the one-CTA form.
-//   full[s]   (even CTA): the producers of both CTAs land their halves on it; the
-//             even producer posts the expected bytes of both;
-//   empty[s]  (both CTAs): the MMA commit arrives on both, multicast;
-//   tfull[a]  (both CTAs): the tile's last commit, multicast;
-//   tempty[a] (even CTA): the 16 epilogue warps of both CTAs arrive on it.
-// ---------------------------------------------------------------------------
 template <bool kOsq, int kStages>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ns_tc_pair_kernel(const __grid_constant__ NsParams p) {
