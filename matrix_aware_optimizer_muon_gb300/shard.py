@@ -63,15 +63,13 @@ def refresh_owners(shapes: Sequence[Tuple[int, int]], world: int) -> List[int]:
 
 
 def step_comm_bytes(shapes: Sequence[Tuple[int, int]], world: int, refresh: bool, x_bytes: int = 2) -> Dict[str, int]:
-    """Bytes one rank sends per step under the plan (for sizing, not measured).
-    RowNorm steps: the rank's column partials of every tall matrix, gathered to all
-    ranks (fp32).  Refresh steps: each matrix's non-owner shards sent to its owner as
-    bf16 X~, and the owner's result rows sent back (bf16)."""
+    """Bytes a rank sends per step under the plan (for sizing, not measured).
+    RowNorm steps: the rank's column partials of every tall matrix, sent to each other
+    rank (fp32).  Refresh steps, averaged over the ranks: each matrix's shards held
+    outside its owner go to the owner as bf16 X~ (a fraction (world - 1)/world of the
+    matrix), and the owner's result rows come back (bf16)."""
     if not refresh:
         cols = sum(c for (r, c) in shapes if needs_column_exchange(r, c))
         return {"column_partials": 4 * cols * (world - 1)}
-    owners = refresh_owners(shapes, world)
-    total = 0
-    for (r, c), o in zip(shapes, owners):
-        total += 2 * r * c * x_bytes * (world - 1) // world   # gather to the owner, scatter back
+    total = sum(2 * r * c * x_bytes * (world - 1) // world for (r, c) in shapes)   # gather + scatter
     return {"gather_scatter": total // world}
