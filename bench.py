@@ -38,7 +38,7 @@ L2_BYTES = 129e6
 # same shape mix (whole MMDiT blocks), scaled by the matrix count of the full set.
 # Valid only for the kernel sources it was measured on (hash below); otherwise the
 # roofline reports null.
-NS5_TRAFFIC = {"mmdit-15b": {"bytes_per_launch": 6.166e10, "sources": "57973f4fb81fce56"}}
+NS5_TRAFFIC = {"mmdit-15b": {"bytes_per_launch": 6.161e10, "sources": "bf84e40d372c8c13"}}
 NS5_SOURCES = ["ns_tc.cu", "ns_common.cuh", "ptx.cuh", "common.cuh", "internal.h", "api.cu"]
 
 

@@ -372,7 +372,6 @@ cudaError_t launch_nz_rms(const NzRmsParams& p, cudaStream_t s);
 cudaError_t launch_apply_ws(int w_dt, int o_dt, const ApplyWsParams& p, cudaStream_t s);
 cudaError_t launch_ns_simt(const NsParams& p, cudaStream_t s);
 cudaError_t launch_ns_tc(const NsParams& p, cudaStream_t s, int num_sms);
-int ns_tc_smem_bytes();
 
 // tensor map encoding (driver entry point obtained through the runtime)
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,

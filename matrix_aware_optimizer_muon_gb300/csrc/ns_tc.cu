@@ -42,7 +42,6 @@ namespace muon {
 namespace tc {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;        // mainloop ring depth; 3 for the launches listed at launch_ns_tc
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -55,7 +54,6 @@ constexpr int SMEM_LIMIT = 227 * 1024;
 // Dynamic shared memory of a launch: the operand ring, the 1 KB alignment slack of the
 // swizzled ring, the barriers.
 constexpr int smem_bytes(int stage_bytes, int stages) { return stages * stage_bytes + 1024 + BAR_BYTES; }
-constexpr int SMEM_BYTES = smem_bytes(STAGE_BYTES, STAGES);
 
 struct Tile {
   int g, mat, tm, tn;
@@ -775,8 +773,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 }
 
 }  // namespace tc
-
-int ns_tc_smem_bytes() { return tc::SMEM_BYTES; }
 
 // Kernel attributes (dynamic shared memory beyond 48 KB) apply per device for the
 // whole process: set once per device, under a lock, with the number of CTA pairs

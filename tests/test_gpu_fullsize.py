@@ -6,8 +6,8 @@ import pytest
 import torch
 
 from oracle import muon_ref
-from parity_util import (TOL_NS5_BF16, TOL_NS5_F32, apply_terms, assert_bf16_close, assert_f32_close, dev,
-                         inputs, to_dev, to_np)
+from parity_util import (TOL_NS5_BF16, TOL_NS5_F32, apply_terms, assert_bf16_close, assert_f32_close,
+                         check_implied_direction, dev, inputs, to_dev, to_np)
 from synth import WORKLOADS, gradient_np, gradient_torch, quantize_np, weight_init_np, weight_init_torch
 
 pytestmark = pytest.mark.gpu
@@ -15,7 +15,13 @@ pytestmark = pytest.mark.gpu
 mm = pytest.importorskip("matrix_aware_optimizer_muon_gb300")
 
 
-def check_step_w(got, refW, prevW, refresh, w_dtype, ns_mode, refM=None):
+def oracle_step(prevW, prevM, G, t, w_dtype):
+    """The oracle's step with W both as stored (w_dtype) and unrounded (fp64)."""
+    W64, M, refresh = muon_ref.periodic_step(prevW, prevM, G, t, w_dtype="f64")
+    return muon_ref.round_to_storage(W64, w_dtype), W64, M, refresh
+
+
+def check_step_w(got, refW, prevW, refresh, w_dtype, ns_mode, refM=None, refW64=None):
     if not refresh:
         if w_dtype == "f32":
             assert_f32_close(got, refW, what="W rownorm step")
@@ -29,6 +35,12 @@ def check_step_w(got, refW, prevW, refresh, w_dtype, ns_mode, refM=None):
     err = np.linalg.norm(got - refW)
     lim = tol * np.linalg.norm(refW - prevW) + np.linalg.norm(np.abs(refW)) * ulp
     assert err <= lim, (err, lim)
+    if refW64 is not None and w_dtype == "bf16":
+        # the direction the fused apply used, within the NS5 tolerance plus half a bf16
+        # ulp of W per element (the bound above lets the W rounding hide O's error)
+        a, b = refW.shape
+        check_implied_direction(got, prevW, refW64, 0.02, 0.01, muon_ref.update_scale(a, b, True, 0.15), tol,
+                                what=f"implied O {a}x{b}")
 
 
 def test_fp32_single_matrix_three_steps():
@@ -83,10 +95,10 @@ def test_bf16_64x1536_six_steps_sampled():
         torch.cuda.synchronize()
         for i in sample:
             prevW = refW[i]
-            refW[i], refM[i], refresh = muon_ref.periodic_step(refW[i], refM[i], Gn[i], t, w_dtype="bf16")
+            refW[i], refW64, refM[i], refresh = oracle_step(refW[i], refM[i], Gn[i], t, "bf16")
             assert br == int(refresh)
             assert_f32_close(to_np(M[i]), refM[i], what=f"M {i} step {t}")
-            check_step_w(to_np(W[i]), refW[i], prevW, refresh, "bf16", "bf16", refM[i])
+            check_step_w(to_np(W[i]), refW[i], prevW, refresh, "bf16", "bf16", refM[i], refW64)
     assert mm.muon_check_status(ws) == mm.MUON_OK
 
 
@@ -116,10 +128,10 @@ def test_mmdit_1_3b_full_set_one_period():
         torch.cuda.synchronize()
         for i in sample:
             prevW = refW[i]
-            refW[i], refM[i], refresh = muon_ref.periodic_step(refW[i], refM[i], Gn[i], t, w_dtype="bf16")
+            refW[i], refW64, refM[i], refresh = oracle_step(refW[i], refM[i], Gn[i], t, "bf16")
             assert br == int(refresh)
             assert_f32_close(to_np(M[i]), refM[i], what=f"M {shapes[i]} step {t}")
-            check_step_w(to_np(W[i]), refW[i], prevW, refresh, "bf16", "bf16", refM[i])
+            check_step_w(to_np(W[i]), refW[i], prevW, refresh, "bf16", "bf16", refM[i], refW64)
         del G
     assert mm.muon_check_status(ws) == mm.MUON_OK
 
@@ -170,10 +182,10 @@ def _sampled_period(wl_key, sample_shapes, seed, steps=3):
         torch.cuda.synchronize()
         for i in sample:
             prevW = refW[i]
-            refW[i], refM[i], refresh = muon_ref.periodic_step(refW[i], refM[i], Gn[i], t, w_dtype="bf16")
+            refW[i], refW64, refM[i], refresh = oracle_step(refW[i], refM[i], Gn[i], t, "bf16")
             assert br == int(refresh)
             assert_f32_close(to_np(M[i]), refM[i], what=f"M {shapes[i]} step {t}")
-            check_step_w(to_np(W[i]), refW[i], prevW, refresh, "bf16", "bf16", refM[i])
+            check_step_w(to_np(W[i]), refW[i], prevW, refresh, "bf16", "bf16", refM[i], refW64)
     assert mm.muon_check_status(ws) == mm.MUON_OK
     del W, M, G, ws
     torch.cuda.empty_cache()
