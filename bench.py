@@ -69,6 +69,8 @@ def parse():
     ap.add_argument("--full-oracle", action="store_true",
                     help="reference arm: also time the oracle over every matrix of the set for one period")
     ap.add_argument("--no-vanilla", action="store_true", help="skip the vanilla Muon (K=1) side-by-side timing")
+    ap.add_argument("--copy-streams", type=int, default=1,
+                    help="e2e: streams (copy engines) each way that a step's upload and download are split over")
     ap.add_argument("--debug-flags", type=int, default=0,
                     help="library test-hook flags for A/B timing (for example 16: one-CTA Newton-Schulz tiles)")
     ap.add_argument("--matrices", type=int, default=0,
@@ -647,63 +649,80 @@ def run_ours(args, torch):
         W_stage = [torch.empty_like(W_flat) for _ in range(NW)]
         G_views = [[gb[o:o + a * b].view(a, b) for o, (a, b) in zip(offs, shapes)] for gb in G_bufs]
         comp = torch.cuda.current_stream()
-        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        # Each step's upload and download are split into CS contiguous pieces on CS
+        # streams each way, so that several copy engines move them at once.
+        CS = max(1, args.copy_streams)
+        cut = [((tot * c // CS) // 128) * 128 for c in range(CS)] + [tot]
+        pieces = [(cut[c], cut[c + 1]) for c in range(CS) if cut[c + 1] > cut[c]]
+        ups = [torch.cuda.Stream() for _ in pieces]
+        downs = [torch.cuda.Stream() for _ in pieces]
         torch.cuda.synchronize()
         n_e2e = max(1, args.steps) * wl.K   # the device-timed region's optimizer steps
-        uploaded = [torch.cuda.Event() for _ in range(NG)]
+        uploaded = [[torch.cuda.Event() for _ in pieces] for _ in range(NG)]
         consumed = [torch.cuda.Event() for _ in range(NG)]
         staged = [torch.cuda.Event() for _ in range(NW)]
-        downloaded = [torch.cuda.Event() for _ in range(NW)]
+        downloaded = [[torch.cuda.Event() for _ in pieces] for _ in range(NW)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
         def upload(j):   # step j's gradients into buffer j % NG, once step j - NG has used it
-            with torch.cuda.stream(up):
-                if j >= NG:
-                    up.wait_event(consumed[j % NG])
-                G_bufs[j % NG].copy_(G_host, non_blocking=True)
-                uploaded[j % NG].record(up)
+            for q, (lo, hi) in enumerate(pieces):
+                s_ = ups[q]
+                with torch.cuda.stream(s_):
+                    if j >= NG:
+                        s_.wait_event(consumed[j % NG])
+                    G_bufs[j % NG][lo:hi].copy_(G_host[lo:hi], non_blocking=True)
+                    uploaded[j % NG][q].record(s_)
+
+        def download(k):   # stage buffer k to the host, once it is staged
+            for q, (lo, hi) in enumerate(pieces):
+                s_ = downs[q]
+                with torch.cuda.stream(s_):
+                    s_.wait_event(staged[k])
+                    W_host[lo:hi].copy_(W_stage[k][lo:hi], non_blocking=True)
+                    downloaded[k][q].record(s_)
 
         barrier(dist)
         e0.record(comp)
-        up.wait_event(e0)
-        down.wait_event(e0)
+        for s_ in ups + downs:
+            s_.wait_event(e0)
         for j in range(min(NG - 1, n_e2e)):
             upload(j)
         for i in range(n_e2e):
             if i + NG - 1 < n_e2e:
                 upload(i + NG - 1)
-            comp.wait_event(uploaded[i % NG])
+            for ev in uploaded[i % NG]:
+                comp.wait_event(ev)
             mm.muon_periodic_step(W, G_views[i % NG], M, step_counter[0], ws, K=wl.K, gamma=wl.gamma, mu=wl.mu,
                                   eta=wl.eta, lam=wl.lam, ns5_mode=mode, scale_mode=args.scale_mode)
             step_counter[0] += 1
             consumed[i % NG].record(comp)
             k = i % NW
             if i >= NW:
-                comp.wait_event(downloaded[k])   # stage buffer k is free once step i - NW's download is done
+                for ev in downloaded[k]:   # stage buffer k is free once step i - NW's download is done
+                    comp.wait_event(ev)
             # Staged by an SM kernel (x * 1 is exact): a device-to-device memcpy takes a
             # copy engine, and the downloads it overlapped slowed from 15.9 to 18-20 ms.
             torch.mul(W_flat, 1, out=W_stage[k])
             staged[k].record(comp)
-            with torch.cuda.stream(down):
-                down.wait_event(staged[k])
-                W_host.copy_(W_stage[k], non_blocking=True)
-                downloaded[k].record(down)
-        comp.wait_stream(down)
+            download(k)
+        for s_ in downs:
+            comp.wait_stream(s_)
         e1.record(comp)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / n_e2e, device)
         # The same copies with no compute between them: the floor the host link sets.
         l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         l0.record(comp)
-        for s_, is_up in ((up, True), (down, False)):
-            with torch.cuda.stream(s_):
-                s_.wait_event(l0)
-                for i in range(n_e2e):
-                    if is_up:
-                        G_bufs[i % NG].copy_(G_host, non_blocking=True)
-                    else:
-                        W_host.copy_(W_stage[i % NW], non_blocking=True)
-            comp.wait_stream(s_)
+        for q, (lo, hi) in enumerate(pieces):
+            for s_, is_up in ((ups[q], True), (downs[q], False)):
+                with torch.cuda.stream(s_):
+                    s_.wait_event(l0)
+                    for i in range(n_e2e):
+                        if is_up:
+                            G_bufs[i % NG][lo:hi].copy_(G_host[lo:hi], non_blocking=True)
+                        else:
+                            W_host[lo:hi].copy_(W_stage[i % NW][lo:hi], non_blocking=True)
+                comp.wait_stream(s_)
         l1.record(comp)
         torch.cuda.synchronize()
         link_ms = max_over_ranks(torch, dist, l0.elapsed_time(l1) / n_e2e, device)
@@ -711,8 +730,10 @@ def run_ours(args, torch):
                        "d2h_bytes_per_step": tot * wb, "steps": n_e2e,
                        "copies_alone_ms": round(link_ms, 4),
                        "copies_alone_gbs": round((tot * gb + tot * wb) / link_ms / 1e6, 1),
+                       "copy_streams": len(pieces),
                        "note": "G uploaded and W downloaded every step from/to pinned host memory, "
-                               f"pipelined with compute ({NG} device buffers for G, {NW} for staging W); "
+                               f"pipelined with compute ({NG} device buffers for G, {NW} for staging W; each "
+                               f"step's copies split over {len(pieces)} streams each way); "
                                "the timed region holds one pipeline fill (first upload) and drain (last "
                                "download); copies_alone_ms: the same copies with no compute"}
 
