@@ -69,8 +69,11 @@ def parse():
     ap.add_argument("--full-oracle", action="store_true",
                     help="reference arm: also time the oracle over every matrix of the set for one period")
     ap.add_argument("--no-vanilla", action="store_true", help="skip the vanilla Muon (K=1) side-by-side timing")
-    ap.add_argument("--copy-streams", type=int, default=1,
-                    help="e2e: streams (copy engines) each way that a step's upload and download are split over")
+    ap.add_argument("--e2e-buckets", type=int, default=16,
+                    help="e2e: buckets of consecutive matrices a step is streamed in (one library call each)")
+    ap.add_argument("--e2e-slots", type=int, default=0,
+                    help="e2e: device buffers for gradient buckets (uploads run up to slots - 1 buckets ahead); "
+                         "0: as many as device memory holds, up to two steps' worth")
     ap.add_argument("--debug-flags", type=int, default=0,
                     help="library test-hook flags for A/B timing (for example 16: one-CTA Newton-Schulz tiles)")
     ap.add_argument("--matrices", type=int, default=0,
@@ -362,6 +365,139 @@ def full_oracle_period(wl, seed=0):
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
+def e2e_buckets(offs, tot, nb):
+    """Split the matrix list into at most nb runs of consecutive matrices holding about
+    equal bytes: [(first matrix, end matrix, first element, end element)]."""
+    ends = offs[1:] + [tot]
+    cuts, k = [0], 1
+    for j, e in enumerate(ends):
+        if k < nb and e >= tot * k / nb and j + 1 < len(offs):
+            cuts.append(j + 1)
+            while k < nb and e >= tot * k / nb:
+                k += 1
+    cuts.append(len(offs))
+    return [(a, b, offs[a], ends[b - 1]) for a, b in zip(cuts, cuts[1:]) if b > a]
+
+
+def run_e2e(args, torch, mm, dist, device, wl, shapes, offs, tot, W_flat, G_flat, W, M, ws, mode, step_counter,
+            gdt, wdt, gb, wb):
+    """The optimizer step end to end through the public call: every step uploads its
+    gradients from pinned host memory and downloads the updated weights to pinned host
+    memory, both inside the timed region.  The matrices are taken in buckets of
+    consecutive matrices (one muon_periodic_step call each), the way a training loop
+    would stream them, so that bucket b's copies overlap the other buckets' compute."""
+    buckets = e2e_buckets(offs, tot, max(1, args.e2e_buckets))
+    span = max(e - s for (_, _, s, e) in buckets)
+    torch.cuda.empty_cache()
+    free = torch.cuda.mem_get_info(device)[0]
+    # G slots: a ring of device buffers of one bucket each, so that uploads run up to
+    # nslot - 1 buckets ahead of the compute.  A refresh step computes for about as long
+    # as two steps' copies take, so the uploads of the following steps must be able to
+    # run that far ahead of it: by default as many slots as fit, up to two steps' worth.
+    want = args.e2e_slots if args.e2e_slots > 0 else 2 * len(buckets) + 1
+    nslot = 0
+    for k in range(want, 0, -1):
+        if k * span * gb + (2 << 30) <= free:
+            nslot = k
+            break
+    if nslot == 0:
+        return {"value": None, "unit": "ms",
+                "skipped": f"not enough device memory for one gradient bucket ({free / 1e9:.1f} GB free, "
+                           f"{(span * gb + (2 << 30)) / 1e9:.1f} GB needed)"}
+    # pinned host copies of G and W (60 GB per rank at 15B): several replicas on one
+    # node may not find that much page-locked memory; then the leg reports why
+    try:
+        G_host = torch.empty(tot, dtype=gdt, pin_memory=True)
+        W_host = torch.empty(tot, dtype=wdt, pin_memory=True)
+    except RuntimeError as exc:
+        return {"value": None, "unit": "ms", "skipped": f"pinned host buffers not available: {str(exc)[:160]}"}
+    G_host.copy_(G_flat)
+    slots = [torch.empty(span, dtype=gdt, device=device) for _ in range(nslot)]
+    views = [[[sl[offs[j] - s0:offs[j] - s0 + shapes[j][0] * shapes[j][1]].view(*shapes[j]) for j in range(a, b)]
+              for (a, b, s0, _) in buckets] for sl in slots]
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    nb = len(buckets)
+    n_e2e = max(1, args.steps) * wl.K   # the device-timed region's optimizer steps
+    items = n_e2e * nb                  # item q: step q // nb, bucket q % nb
+    uploaded = [torch.cuda.Event() for _ in range(nslot)]
+    consumed = [torch.cuda.Event() for _ in range(nslot)]
+    updated = [torch.cuda.Event() for _ in range(nb)]
+    downloaded = [torch.cuda.Event() for _ in range(nb)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def upload(q):   # item q's gradients into slot q % nslot, once item q - nslot has read that slot
+        a, b, s0, s1 = buckets[q % nb]
+        with torch.cuda.stream(up):
+            if q >= nslot:
+                up.wait_event(consumed[q % nslot])
+            slots[q % nslot][:s1 - s0].copy_(G_host[s0:s1], non_blocking=True)
+            uploaded[q % nslot].record(up)
+
+    def download(q):   # bucket q % nb's updated weights to the host
+        a, b, s0, s1 = buckets[q % nb]
+        with torch.cuda.stream(down):
+            down.wait_event(updated[q % nb])
+            W_host[s0:s1].copy_(W_flat[s0:s1], non_blocking=True)
+            downloaded[q % nb].record(down)
+
+    barrier(dist)
+    e0.record(comp)
+    up.wait_event(e0)
+    down.wait_event(e0)
+    for q in range(min(nslot - 1, items)):
+        upload(q)
+    for q in range(items):
+        if q + nslot - 1 < items:
+            upload(q + nslot - 1)
+        i, bk = divmod(q, nb)
+        a, b, _, _ = buckets[bk]
+        comp.wait_event(uploaded[q % nslot])
+        if i >= 1:   # the previous step's download of these weights must have read them
+            comp.wait_event(downloaded[bk])
+        mm.muon_periodic_step(W[a:b], views[q % nslot][bk], M[a:b], step_counter[0] + i, ws, K=wl.K,
+                              gamma=wl.gamma, mu=wl.mu, eta=wl.eta, lam=wl.lam, ns5_mode=mode,
+                              scale_mode=args.scale_mode)
+        consumed[q % nslot].record(comp)
+        updated[bk].record(comp)
+        download(q)
+    comp.wait_stream(down)
+    e1.record(comp)
+    torch.cuda.synchronize()
+    step_counter[0] += n_e2e
+    if mm.muon_check_status(ws) != mm.MUON_OK:
+        raise RuntimeError("device status error in the end-to-end run")
+    e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / n_e2e, device)
+    # The same copies with no compute between them: the floor the host link sets.
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(comp)
+    for s_, is_up in ((up, True), (down, False)):
+        with torch.cuda.stream(s_):
+            s_.wait_event(l0)
+            for q in range(items):
+                a, b, s0, s1 = buckets[q % nb]
+                if is_up:
+                    slots[q % nslot][:s1 - s0].copy_(G_host[s0:s1], non_blocking=True)
+                else:
+                    W_host[s0:s1].copy_(W_flat[s0:s1], non_blocking=True)
+        comp.wait_stream(s_)
+    l1.record(comp)
+    torch.cuda.synchronize()
+    link_ms = max_over_ranks(torch, dist, l0.elapsed_time(l1) / n_e2e, device)
+    return {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": tot * gb,
+            "d2h_bytes_per_step": tot * wb, "steps": n_e2e,
+            "copies_alone_ms": round(link_ms, 4),
+            "copies_alone_gbs": round((tot * gb + tot * wb) / link_ms / 1e6, 1),
+            "buckets": nb, "gradient_slots": nslot,
+            "note": "every step: G uploaded from and W downloaded to pinned host memory, "
+                    f"in {nb} buckets of consecutive matrices (one muon_periodic_step call each; "
+                    f"{nslot} device slots for G buckets, so uploads run ahead of the compute; "
+                    "a bucket's download overlaps the next buckets' compute); the timed region "
+                    "holds one pipeline fill (first upload) and drain (last download); "
+                    "copies_alone_ms: the same copies with no compute"}
+
+
 def run_ours(args, torch):
     import matrix_aware_optimizer_muon_gb300 as mm
     from synth import WORKLOADS, gradient_torch, weight_init_torch
@@ -572,12 +708,6 @@ def run_ours(args, torch):
             "optimizer_time_cut": round(1.0 - line["value"] / v_ms, 4),
             "clocks": vclk}
 
-    # End to end through the public API with host buffers (pinned): every optimizer step
-    # uploads its gradients and downloads its updated weights inside the timed region.
-    # Copies are pipelined with compute the way a training loop would run them: G has
-    # NG device buffers, so uploads run up to NG - 1 steps ahead (through a long refresh
-    # step too), and W is staged into one of NW device buffers after each step, so that
-    # its download overlaps the following steps.
     # Per-branch timing as CUDA-graph replays: one refresh step and one RowNorm step are
     # each captured once and replayed 20 times (the median of the per-replay event
     # times is reported).  Replays repeat the same step on the same buffers, which is
@@ -625,124 +755,9 @@ def run_ours(args, torch):
         except RuntimeError as exc:   # capture unsupported here: leave the field out, say why
             line["graph"] = {"skipped": str(exc)[:200]}
 
-    e2e_bufs = None
     if not args.no_e2e:
-        torch.cuda.empty_cache()
-        free = torch.cuda.mem_get_info(device)[0]
-        # fewer staging buffers when device memory is short (the 15B set: W, G, M and the
-        # workspace hold about 245 GB); with one G buffer the next upload waits for the
-        # step that reads it, so copies overlap compute less
-        for ng, nw in ((3, 2), (2, 1), (1, 1)):
-            if (ng - 1) * tot * gb + nw * tot * wb + (1 << 30) <= free:
-                e2e_bufs = (ng, nw)
-                break
-        if e2e_bufs is None:
-            line["e2e"] = {"value": None, "unit": "ms",
-                           "skipped": f"not enough device memory for the staging buffers ({free / 1e9:.1f} GB free, "
-                                      f"{(tot * wb + (1 << 30)) / 1e9:.1f} GB needed at least)"}
-    if e2e_bufs is not None:
-        NG, NW = e2e_bufs
-        # pinned host copies of G and W (60 GB per rank at 15B): several replicas on one
-        # node may not find that much page-locked memory; then the leg reports why
-        try:
-            G_host = torch.empty(tot, dtype=gdt, pin_memory=True)
-            W_host = torch.empty(tot, dtype=wdt, pin_memory=True)
-        except RuntimeError as exc:
-            line["e2e"] = {"value": None, "unit": "ms", "skipped": f"pinned host buffers not available: {str(exc)[:160]}"}
-            e2e_bufs = None
-    if e2e_bufs is not None:
-        G_host.copy_(G_flat)
-        G_bufs = [G_flat] + [torch.empty_like(G_flat) for _ in range(NG - 1)]
-        W_stage = [torch.empty_like(W_flat) for _ in range(NW)]
-        G_views = [[gb[o:o + a * b].view(a, b) for o, (a, b) in zip(offs, shapes)] for gb in G_bufs]
-        comp = torch.cuda.current_stream()
-        # Each step's upload and download are split into CS contiguous pieces on CS
-        # streams each way, so that several copy engines move them at once.
-        CS = max(1, args.copy_streams)
-        cut = [((tot * c // CS) // 128) * 128 for c in range(CS)] + [tot]
-        pieces = [(cut[c], cut[c + 1]) for c in range(CS) if cut[c + 1] > cut[c]]
-        ups = [torch.cuda.Stream() for _ in pieces]
-        downs = [torch.cuda.Stream() for _ in pieces]
-        torch.cuda.synchronize()
-        n_e2e = max(1, args.steps) * wl.K   # the device-timed region's optimizer steps
-        uploaded = [[torch.cuda.Event() for _ in pieces] for _ in range(NG)]
-        consumed = [torch.cuda.Event() for _ in range(NG)]
-        staged = [torch.cuda.Event() for _ in range(NW)]
-        downloaded = [[torch.cuda.Event() for _ in pieces] for _ in range(NW)]
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
-        def upload(j):   # step j's gradients into buffer j % NG, once step j - NG has used it
-            for q, (lo, hi) in enumerate(pieces):
-                s_ = ups[q]
-                with torch.cuda.stream(s_):
-                    if j >= NG:
-                        s_.wait_event(consumed[j % NG])
-                    G_bufs[j % NG][lo:hi].copy_(G_host[lo:hi], non_blocking=True)
-                    uploaded[j % NG][q].record(s_)
-
-        def download(k):   # stage buffer k to the host, once it is staged
-            for q, (lo, hi) in enumerate(pieces):
-                s_ = downs[q]
-                with torch.cuda.stream(s_):
-                    s_.wait_event(staged[k])
-                    W_host[lo:hi].copy_(W_stage[k][lo:hi], non_blocking=True)
-                    downloaded[k][q].record(s_)
-
-        barrier(dist)
-        e0.record(comp)
-        for s_ in ups + downs:
-            s_.wait_event(e0)
-        for j in range(min(NG - 1, n_e2e)):
-            upload(j)
-        for i in range(n_e2e):
-            if i + NG - 1 < n_e2e:
-                upload(i + NG - 1)
-            for ev in uploaded[i % NG]:
-                comp.wait_event(ev)
-            mm.muon_periodic_step(W, G_views[i % NG], M, step_counter[0], ws, K=wl.K, gamma=wl.gamma, mu=wl.mu,
-                                  eta=wl.eta, lam=wl.lam, ns5_mode=mode, scale_mode=args.scale_mode)
-            step_counter[0] += 1
-            consumed[i % NG].record(comp)
-            k = i % NW
-            if i >= NW:
-                for ev in downloaded[k]:   # stage buffer k is free once step i - NW's download is done
-                    comp.wait_event(ev)
-            # Staged by an SM kernel (x * 1 is exact): a device-to-device memcpy takes a
-            # copy engine, and the downloads it overlapped slowed from 15.9 to 18-20 ms.
-            torch.mul(W_flat, 1, out=W_stage[k])
-            staged[k].record(comp)
-            download(k)
-        for s_ in downs:
-            comp.wait_stream(s_)
-        e1.record(comp)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / n_e2e, device)
-        # The same copies with no compute between them: the floor the host link sets.
-        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        l0.record(comp)
-        for q, (lo, hi) in enumerate(pieces):
-            for s_, is_up in ((ups[q], True), (downs[q], False)):
-                with torch.cuda.stream(s_):
-                    s_.wait_event(l0)
-                    for i in range(n_e2e):
-                        if is_up:
-                            G_bufs[i % NG][lo:hi].copy_(G_host[lo:hi], non_blocking=True)
-                        else:
-                            W_host[lo:hi].copy_(W_stage[i % NW][lo:hi], non_blocking=True)
-                comp.wait_stream(s_)
-        l1.record(comp)
-        torch.cuda.synchronize()
-        link_ms = max_over_ranks(torch, dist, l0.elapsed_time(l1) / n_e2e, device)
-        line["e2e"] = {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": tot * gb,
-                       "d2h_bytes_per_step": tot * wb, "steps": n_e2e,
-                       "copies_alone_ms": round(link_ms, 4),
-                       "copies_alone_gbs": round((tot * gb + tot * wb) / link_ms / 1e6, 1),
-                       "copy_streams": len(pieces),
-                       "note": "G uploaded and W downloaded every step from/to pinned host memory, "
-                               f"pipelined with compute ({NG} device buffers for G, {NW} for staging W; each "
-                               f"step's copies split over {len(pieces)} streams each way); "
-                               "the timed region holds one pipeline fill (first upload) and drain (last "
-                               "download); copies_alone_ms: the same copies with no compute"}
+        line["e2e"] = run_e2e(args, torch, mm, dist, device, wl, shapes, offs, tot, W_flat, G_flat, W, M, ws, mode,
+                              step_counter, gdt, wdt, gb, wb)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t0c = time.perf_counter()

@@ -358,7 +358,8 @@ def test_refresh_step_more_groups_and_matrices_than_one_launch_takes(mode):
 # ---------------------------------------------------------------------------
 # schedule, determinism, resume, vanilla Muon
 # ---------------------------------------------------------------------------
-def run_steps(shapes, dt, steps, K=3, mode="bf16", start_state=None, start_step=0, seed=0):
+def run_steps(shapes, dt, steps, K=3, mode="bf16", start_state=None, start_step=0, seed=0, buckets=None):
+    """buckets: [(first, end)] runs of the matrix list, each taken by its own call."""
     W0, Gs = inputs(shapes, dt, dt, start_step + steps, seed=seed)
     if start_state is None:
         W = [to_dev(w, dt) for w in W0]
@@ -369,7 +370,12 @@ def run_steps(shapes, dt, steps, K=3, mode="bf16", start_state=None, start_step=
     branches = []
     for t in range(start_step, start_step + steps):
         G = [to_dev(g, dt) for g in Gs[t]]
-        branches.append(mm.muon_periodic_step(W, G, M, t, ws, K=K, ns5_mode=mode))
+        if buckets is None:
+            branches.append(mm.muon_periodic_step(W, G, M, t, ws, K=K, ns5_mode=mode))
+        else:
+            brs = {mm.muon_periodic_step(W[a:b], G[a:b], M[a:b], t, ws, K=K, ns5_mode=mode) for a, b in buckets}
+            assert len(brs) == 1
+            branches.append(brs.pop())
     torch.cuda.synchronize()
     assert mm.muon_check_status(ws) == mm.MUON_OK
     return W, M, branches
@@ -381,6 +387,19 @@ def test_determinism_bit_exact():
     W2, M2, b2 = run_steps(shapes, "bf16", 4)
     assert b1 == b2 == [1, 0, 0, 1]
     for a, b in zip(W1 + M1, W2 + M2):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("mode", ["bf16", "f32"])
+def test_bucketed_calls_match_one_call(mode):
+    """A step taken in buckets of consecutive matrices (one call each, one workspace, as
+    the end-to-end benchmark streams them) is bit-identical to one call over all: every
+    matrix's arithmetic is its own, whatever else shares the launches."""
+    shapes = [(300, 1000), (1000, 300), (256, 256), (40, 520), (520, 40), (1, 300), (384, 1280), (1280, 384)]
+    Wa, Ma, ba = run_steps(shapes, "bf16", 4, mode=mode)
+    Wb, Mb, bb = run_steps(shapes, "bf16", 4, mode=mode, buckets=[(0, 3), (3, 4), (4, 8)])
+    assert ba == bb == [1, 0, 0, 1]
+    for a, b in zip(Wa + Ma, Wb + Mb):
         assert torch.equal(a, b)
 
 
